@@ -1,0 +1,211 @@
+"""Checks that pin the fp64 oracle to facts outside itself.
+
+Each ``check_*`` function takes an ``oracle.Oracle`` and raises
+``AssertionError`` when the oracle disagrees with:
+
+* hand-derived answers (``tests/golden/hand_cases.json``);
+* an exact-rational brute force (``fractions.Fraction``) on tiny inputs --
+  every bf16 value is a dyadic rational, so the exact argmin is known;
+* the identity ||x - c||^2 = ||x||^2 + s, with the distance computed
+  directly from the difference vector;
+* ``numpy.argmin`` (documented to return the first occurrence) over an exact
+  fp64 score matrix on integer data;
+* closed-form winners for rows holding one infinity;
+* self-consistency of the row-subset and pair-score entry points.
+
+The same functions run against deliberately broken copies of the oracle in
+``test_oracle_mutants.py``: every planted mistake must trip at least one.
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "hand_cases.json")
+
+
+def _val(v):
+    if isinstance(v, str):
+        return {"nan": math.nan, "inf": math.inf, "-inf": -math.inf, "-0": -0.0}[v]
+    return float(v)
+
+
+def _bf16_rows(rows):
+    t = torch.tensor([[_val(v) for v in r] for r in rows], dtype=torch.float32)
+    b = t.to(torch.bfloat16)
+    # the fixtures are exact in bf16: nothing may round
+    back = b.to(torch.float32)
+    same = (back == t) | (torch.isnan(back) & torch.isnan(t))
+    assert bool(same.all()), "golden value not exact in bf16"
+    return b.contiguous()
+
+
+def _same_score(a: float, b: float) -> bool:
+    if math.isnan(a) or math.isnan(b):
+        return math.isnan(a) and math.isnan(b)
+    return a == b
+
+
+def load_golden():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+def check_golden(orc):
+    for case in load_golden():
+        X = _bf16_rows(case["X"])
+        C = _bf16_rows(case["C"])
+        idx, mins = orc.assign(X, C)
+        exp_idx = case["idx"]
+        exp_min = [_val(v) for v in case["minscore"]]
+        assert list(idx) == exp_idx, (case["name"], list(idx), exp_idx)
+        for got, exp in zip(mins, exp_min):
+            assert _same_score(float(got), exp), (case["name"], float(got), exp)
+
+
+def _exact(b16: torch.Tensor):
+    return [[Fraction(float(v)) for v in row] for row in b16.to(torch.float32).tolist()]
+
+
+def _exact_assign(Xf, Cf):
+    """Exact-rational argmin with lowest-index ties (finite inputs only)."""
+    norms = [sum(c * c for c in row) for row in Cf]
+    out_idx, out_s = [], []
+    for x in Xf:
+        s = [norms[j] - 2 * sum(a * b for a, b in zip(x, Cf[j])) for j in range(len(Cf))]
+        m = min(s)
+        j = s.index(m)          # list.index: the first occurrence
+        out_idx.append(j)
+        out_s.append(m)
+    return out_idx, out_s, norms
+
+
+def check_bruteforce_rational(orc, trials: int = 24):
+    rng = np.random.default_rng(12345)
+    for t in range(trials):
+        N = int(rng.integers(1, 9))
+        K = int(rng.integers(1, 13))
+        D = int(rng.integers(1, 17))
+        if t % 3 == 0:
+            X, C = workloads.integers(N, K, D, seed=1000 + t, lo=-2, hi=2)
+        elif t % 3 == 1:
+            X, C = workloads.iid(N, K, D, seed=2000 + t)
+        else:
+            X, C = workloads.blobs(N, K, D, seed=3000 + t)
+            # force cross-index duplicates so exact ties occur
+            if K >= 2:
+                C[K - 1] = C[0]
+        Xf, Cf = _exact(X), _exact(C)
+        exp_idx, exp_s, exp_norms = _exact_assign(Xf, Cf)
+        idx, mins = orc.assign(X, C)
+        assert list(idx) == exp_idx, (t, list(idx), exp_idx)
+        for got, exp in zip(mins, exp_s):
+            # fp64 sums of <= 16 bf16 products are exact here; keep a
+            # rounding-sized allowance in case a sum spans many binades
+            assert abs(Fraction(float(got)) - exp) <= Fraction(1, 2**40) * (1 + abs(exp)), (t, got, exp)
+        norms = orc.norms(C)
+        for got, exp in zip(norms, exp_norms):
+            assert Fraction(float(got)) == exp, (t, got, exp)
+
+
+def check_distance_identity(orc):
+    # float data: ||x - c||^2 computed from the difference vector
+    X, C = workloads.iid(40, 30, 48, seed=77)
+    xs = X.to(torch.float64).numpy()
+    cs = C.to(torch.float64).numpy()
+    ii, jj = np.meshgrid(np.arange(40), np.arange(30), indexing="ij")
+    ii, jj = ii.ravel(), jj.ravel()
+    s = orc.scores(X, C, ii, jj)
+    diff = xs[ii] - cs[jj]
+    dist = np.einsum("pd,pd->p", diff, diff)
+    xn = np.einsum("pd,pd->p", xs[ii], xs[ii])
+    cn = np.einsum("pd,pd->p", cs[jj], cs[jj])
+    err = np.abs((xn + s) - dist)
+    assert np.all(err <= 1e-12 * (xn + cn + 1.0)), float(err.max())
+    # integer data: the identity holds exactly
+    X, C = workloads.integers(25, 19, 33, seed=78)
+    xs = X.to(torch.float64).numpy()
+    cs = C.to(torch.float64).numpy()
+    ii, jj = np.meshgrid(np.arange(25), np.arange(19), indexing="ij")
+    ii, jj = ii.ravel(), jj.ravel()
+    s = orc.scores(X, C, ii, jj)
+    diff = xs[ii] - cs[jj]
+    dist = np.einsum("pd,pd->p", diff, diff)
+    xn = np.einsum("pd,pd->p", xs[ii], xs[ii])
+    assert np.array_equal(xn + s, dist)
+    # the winner is the nearest centroid in Euclidean distance
+    idx, _ = orc.assign(X, C)
+    full = ((xs[:, None, :] - cs[None, :, :]) ** 2).sum(-1)
+    assert np.array_equal(idx, np.argmin(full, axis=1))
+
+
+def check_numpy_argmin(orc):
+    for seed, (N, K, D) in enumerate([(200, 97, 24), (64, 300, 8), (33, 5, 64)]):
+        X, C = workloads.integers(N, K, D, seed=500 + seed)
+        if K > 4:
+            C[K // 2:K // 2 + 3] = C[1]        # ties far apart in the index
+        xs = X.to(torch.float64).numpy()
+        cs = C.to(torch.float64).numpy()
+        S = (cs * cs).sum(1)[None, :] - 2.0 * (xs @ cs.T)   # exact on integers
+        idx, mins = orc.assign(X, C)
+        exp = np.argmin(S, axis=1)                          # first occurrence
+        assert np.array_equal(idx, exp), seed
+        assert np.array_equal(mins, S[np.arange(N), exp]), seed
+
+
+def check_single_infinity_rows(orc):
+    """Closed form for a row with one +-inf at dimension d, finite elsewhere.
+
+    x.c_j is +inf * sign(c_jd) (NaN when c_jd == 0), so s_j is -inf where
+    x_d * c_jd > 0, +inf where < 0 and NaN where c_jd == 0.  Winner: the
+    lowest j with -inf, else the lowest j with +inf, else 0 (all NaN).
+    """
+    rng = np.random.default_rng(7)
+    for t in range(30):
+        K = int(rng.integers(1, 12))
+        D = int(rng.integers(1, 6))
+        X, C = workloads.integers(1, K, D, seed=900 + t, lo=-1, hi=1)
+        d = int(rng.integers(0, D))
+        sign = 1.0 if t % 2 == 0 else -1.0
+        X[0, d] = sign * math.inf
+        col = C[:, d].to(torch.float32).numpy() * sign
+        neg = np.nonzero(col > 0)[0]
+        pos = np.nonzero(col < 0)[0]
+        if neg.size:
+            exp_j, exp_s = int(neg[0]), -math.inf
+        elif pos.size:
+            exp_j, exp_s = int(pos[0]), math.inf
+        else:
+            exp_j, exp_s = 0, math.nan
+        idx, mins = orc.assign(X, C)
+        assert int(idx[0]) == exp_j, (t, int(idx[0]), exp_j)
+        assert _same_score(float(mins[0]), exp_s), (t, float(mins[0]), exp_s)
+    # NaN anywhere in x makes every score NaN
+    X, C = workloads.integers(3, 9, 7, seed=901)
+    X[1, 3] = math.nan
+    idx, mins = orc.assign(X, C)
+    assert int(idx[1]) == 0 and math.isnan(mins[1])
+
+
+def check_subsets_consistent(orc):
+    X, C = workloads.blobs(50, 20, 12, seed=31)
+    full_idx, full_min = orc.assign(X, C)
+    rows = np.array([49, 0, 7, 7, 23])
+    idx, mins = orc.assign(X, C, rows=rows)
+    assert np.array_equal(idx, full_idx[rows])
+    assert np.array_equal(mins, full_min[rows])
+    s = orc.scores(X, C, rows, full_idx[rows])
+    assert np.array_equal(s, full_min[rows])
+
+
+ALL_CHECKS = [check_golden, check_bruteforce_rational, check_distance_identity,
+              check_numpy_argmin, check_single_infinity_rows, check_subsets_consistent]
