@@ -1,0 +1,458 @@
+"""Benchmark of the k-means assignment step on GB300 (one JSON line).
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+centroid norms (kmassign_norms) + assignment (kmassign), inputs resident in
+HBM.  Default workload: N=262,144 points, D=256, K=16,384 centroids, X and C
+iid N(0,1) in bf16 -- the shape the throughput target is stated on.
+
+Metric: TFLOP/s counted as 2*N*K*D per step (the dense X.C^T the method
+performs), whole job over all ranks.  Three seeded input sets rotate between
+steps (410 MB in total, more than the 126 MB L2), as in the pages' method
+(flashlib PR #22, "Benchmark methodology": three seeded sets rotated between
+calls, warm-up calls, CUDA-event timing).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload KEY]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, same metric
+
+Multi-GPU (torchrun): every rank assigns its own batch of N points against
+the full centroid set (points shard with no exchange), so scaling is weak;
+the only collectives are the timing barrier and a max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "k-means assign TFLOP/s (2*N*K*D / t), 1 pass of norms + assignment"
+UNIT = "TFLOP/s"
+# The pages' own figure for this shape (B200, flashlib PR #22 "Benchmark
+# results": N=262,144, D=256, K=16,384 in 1.8615 ms -> 1,181 TFLOP/s).
+PAGES_B200_TFLOPS = {"iid_normal": 2 * 262144 * 16384 * 256 / 1.8615e-3 / 1e12}
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "assign_kernel_traffic.json")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(kernel_sha: str):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None, None
+    if t.get("source_sha") != kernel_sha:
+        return None, t
+    return t, t
+
+
+def kernel_source_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "means_nearest_centroid_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        target = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            uuid = getattr(props, "uuid", None)
+            if uuid is not None:
+                s = str(uuid)
+                target = s if s.startswith("GPU-") else "GPU-" + s
+        except Exception:
+            target = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if target:
+            cmd += ["-i", target]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                self.samples.append(dict(t=ts, sm=float(parts[1]), smax=float(parts[2]),
+                                         power=float(parts[3]) if parts[3][0].isdigit() else None,
+                                         hw=parts[4] == "Active", hwt=parts[5] == "Active",
+                                         swt=parts[6] == "Active", pcap=parts[7] == "Active"))
+            except (ValueError, IndexError):
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s["t"] <= t1]
+        window = "timed"
+        if not inside:
+            inside = [s for s in self.samples if s["t"] <= t1 + 0.2]
+            window = "warmup+timed"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "none"}
+        reasons = set()
+        for s in inside:
+            if s["hw"]:
+                reasons.add("hw_slowdown")
+            if s["hwt"]:
+                reasons.add("hw_thermal_slowdown")
+            if s["swt"]:
+                reasons.add("sw_thermal_slowdown")
+            if s["pcap"]:
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(s["sm"] for s in inside),
+                "sm_max_mhz": max(s["smax"] for s in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+def make_inputs(key, variants, device):
+    sets = []
+    for v in range(variants):
+        X, C = workloads.make(key, variant=v)
+        sets.append((X, C))
+    dev_sets = [(X.to(device), C.to(device)) for X, C in sets]
+    return sets, dev_sets
+
+
+def cpu_oracle_rate(X, C, budget_s: float, max_rows: int | None = None):
+    """Time the fp64 oracle on the first R rows of X against all of C.
+
+    R is picked from a short calibration so the measured run takes about
+    budget_s seconds.  Returns (tflops, rows, seconds, threads).
+    """
+    import oracle
+    orc = oracle.Oracle()
+    threads = orc.max_threads()
+    K, D = C.shape
+    cn = orc.norms(C)
+    probe = max(threads, 8)
+    t0 = time.perf_counter()
+    orc.assign(X[:probe], C, cnorm=cn)
+    dt = time.perf_counter() - t0
+    per_row = dt / probe
+    rows = int(max(threads, min(X.shape[0], budget_s / max(per_row, 1e-9))))
+    if max_rows:
+        rows = min(rows, max_rows)
+    t0 = time.perf_counter()
+    orc.assign(X[:rows], C, cnorm=cn)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * K * D / dt / 1e12, rows, dt, threads
+
+
+def run_reference(args, key):
+    """The fp64 CPU oracle as the reference arm, same metric and config."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = workloads.WORKLOADS[key]
+    X, C = workloads.make(key)
+    import oracle
+    orc = oracle.Oracle()
+    threads = orc.max_threads()
+    cn = orc.norms(C)
+    probe = max(threads, 8)
+    t0 = time.perf_counter()
+    orc.assign(X[:probe], C, cnorm=cn)
+    per_row = (time.perf_counter() - t0) / probe
+    total_budget = args.ref_budget_s
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    rows = int(max(threads, min(w.N, per_step / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        orc.assign(X[:rows], C, cnorm=cn)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        orc.assign(X[:rows], C, cnorm=cn)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = 2.0 * rows * w.K * w.D * args.steps / total / 1e12
+    sample = (f"first {rows} of {w.N} points against all {w.K} centroids per step "
+              f"(fp64 oracle, OpenMP over points)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.text, "key": key, "N": w.N, "D": w.D, "K": w.K,
+                   "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="iid_normal", choices=list(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--ref-budget-s", type=float, default=150.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--parity-rows", type=int, default=256)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    key = args.workload
+    if args.impl == "reference":
+        return run_reference(args, key)
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    else:
+        dist = None
+
+    from means_nearest_centroid_gb300 import _build
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    import means_nearest_centroid_gb300 as km
+    km.library()
+
+    w = workloads.WORKLOADS[key]
+    N, D, K = w.N, w.D, w.K
+    flops = 2.0 * N * K * D
+    sets, dsets = make_inputs(key, 3, device)
+    cns = [torch.empty(K, dtype=torch.float32, device=device) for _ in dsets]
+    idxs = [torch.empty(N, dtype=torch.int32, device=device) for _ in dsets]
+    stream = torch.cuda.current_stream(device)
+    plan = km.kmassign_plan(N, K, D)
+    norms_in_step = not w.precomputed_norms
+    if not norms_in_step:
+        for (X, C), cn in zip(dsets, cns):
+            km.kmassign_norms(C, out=cn, stream=stream)
+
+    def step(i, ev_mid=None, ev_end=None):
+        X, C = dsets[i % 3]
+        if norms_in_step:
+            km.kmassign_norms(C, out=cns[i % 3], stream=stream)
+        if ev_mid is not None:
+            ev_mid.record(stream)
+        km.kmassign(X, C, cnorm=cns[i % 3], idx=idxs[i % 3], stream=stream)
+        if ev_end is not None:
+            ev_end.record(stream)
+
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    rc = km.kmassign_check(stream)
+    if rc != 0:
+        raise SystemExit(f"warm-up failed: {km.kmassign_strerror(rc)}")
+
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, mids[i], ends[i])
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    rc = km.kmassign_check(stream)
+    if rc != 0:
+        raise SystemExit(f"timed run failed: {km.kmassign_strerror(rc)}")
+    sampler.stop()
+    total_ms = t_start.elapsed_time(t_stop)
+    kern_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+    if dist is not None:
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = flops * ws * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel (the assignment kernel)
+    peaks, peak_src = load_peaks()
+    kernel_avg_ms = statistics.mean(kern_ms)
+    kernel_med_ms = statistics.median(kern_ms)
+    achieved = flops / (kernel_avg_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sha = kernel_source_sha()
+    traffic, traffic_rec = load_traffic(sha)
+    traffic_bytes = None
+    if traffic is not None and traffic.get("workload") == key:
+        traffic_bytes = traffic.get("bytes_per_launch")
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic_bytes,
+                "peak_source": f"{peak_src} bf16 dense (burst)",
+                "kernel": "assign_kernel (tcgen05)", "kernel_ms_avg": kernel_avg_ms,
+                "kernel_ms_median": kernel_med_ms,
+                "algorithmic_bytes": N * D * 2 + K * D * 2 + N * 4 + K * 4}
+
+    # ---- parity sample against the oracle (rows computed one by one)
+    parity_info = None
+    if rank == 0 and args.parity_rows > 0:
+        import oracle
+        orc = oracle.Oracle()
+        X0, C0 = sets[0]
+        g = np.random.default_rng(w.seed)
+        rows = np.sort(g.choice(N, min(N, args.parity_rows), replace=False))
+        idx0 = idxs[0].cpu().numpy().astype(np.int64)
+        o_idx, o_min = orc.assign(X0, C0, rows=rows)
+        diff = np.nonzero(idx0[rows] != o_idx)[0]
+        bad = 0
+        if diff.size:
+            s = orc.scores(X0, C0, rows[diff], idx0[rows][diff])
+            xs = X0[rows[diff]].double().numpy()
+            scale = (xs * xs).sum(1) + orc.norms(C0)[idx0[rows][diff]]
+            bad = int(np.sum(~(s - o_min[diff] <= 2e-5 * scale)))
+        parity_info = {"rows": int(rows.size), "idx_differs": int(diff.size),
+                       "outside_tolerance": bad}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        X0, C0 = sets[0]
+        Xh = X0.pin_memory()
+        Ch = C0.pin_memory()
+        idx_h = torch.empty(N, dtype=torch.int32).pin_memory()
+        scratch = {"X": dsets[1][0], "C": dsets[1][1], "idx": idxs[1]}
+        km.assign_host(Xh, Ch, idx_h, device=device, scratch=scratch)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            km.assign_host(Xh, Ch, idx_h, device=device, scratch=scratch)
+        e2e_s = time.perf_counter() - t0
+        if dist is not None:
+            t = torch.tensor([e2e_s], device=device, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": flops * ws * args.e2e_steps / e2e_s / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": Xh.numel() * 2 + Ch.numel() * 2,
+               "d2h_bytes_per_step": idx_h.numel() * 4, "steps": args.e2e_steps,
+               "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
+               "note": "pinned host X and C copied in, norms + assignment, idx copied out, "
+                       "stream synchronised, every step"}
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        X0, C0 = sets[0]
+        rate, rows, secs, threads = cpu_oracle_rate(X0, C0, args.cpu_budget_s)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"first {rows} of {N} points against all {K} centroids, "
+                         f"{secs:.1f} s, fp64 oracle (OpenMP over points)"}
+
+    clocks = sampler.summary(wall0, wall1)
+    launches_per_step = (1 if norms_in_step else 0) + 1 + (1 if plan["ksplit"] > 1 else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": (value / PAGES_B200_TFLOPS[key]) if key in PAGES_B200_TFLOPS else None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.text, "key": key, "N": N, "D": D, "K": K,
+                   "norms_in_step": norms_in_step,
+                   "l2": "3 rotating seeded input sets per GPU, larger than the 126 MB L2 "
+                         "together",
+                   "plan": plan, "parallelism": f"points sharded, {ws} independent batches"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "parity_sample": parity_info,
+    }
+    if traffic_rec is not None and traffic_bytes is None:
+        line["roofline"]["traffic_note"] = "stored ncu traffic is for another kernel revision or workload"
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,130 @@
+/*
+ * kmassign.h -- C ABI of libkmassign, the k-means assignment step on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (flashlib PR #22 "Optimize Blackwell k-means assignment
+ * reduction", Summary): for every point x_i, form the scores of all
+ * centroids from their dot products with x_i, apply the centroid norms, and
+ * select the winning centroid, ties going to the lowest index:
+ *
+ *     s_ij   = ||c_j||^2 - 2 * x_i . c_j
+ *     idx[i] = the lowest j whose s_ij is minimal
+ *
+ * ||x_i||^2 is the same for every j, so idx[i] is the centroid nearest to
+ * x_i in Euclidean distance.  Ordering of scores: -0 equals +0; NaN is above
+ * every number (a NaN score never beats a number, +inf included).  A row whose
+ * scores are all NaN (for example a row holding a NaN) gets idx 0 and minscore
+ * NaN; the pages test NaN rows but fix no convention, this is the one chosen.
+ *
+ * Arithmetic (what the GPU computes): x and c are bf16; x_i . c_j is summed in
+ * fp32 by the tensor cores (order of summation unspecified); ||c_j||^2 is an
+ * fp32 sum of exact bf16 squares; s_ij = fmaf(-2, dot, cnorm_j) in fp32.  On
+ * integer-valued inputs whose sums stay below 2^24 every step is exact.
+ *
+ * Layout: every matrix is row-major and contiguous, D innermost.  Row pitch
+ * is D * 2 bytes.  All pointers are device pointers (cudaMalloc, the stream
+ * allocator or PyTorch CUDA tensors); host or unregistered pointers are
+ * rejected with KMASSIGN_ERR_NOT_DEVICE before anything is launched.
+ *
+ * Ownership: the caller owns every buffer it passes.  The library keeps no
+ * pointer after a call returns.  Temporaries (the norm buffer when cnorm is
+ * NULL, and the packed-key workspace when the centroid range is split across
+ * thread blocks) are taken with cudaMallocAsync and released with
+ * cudaFreeAsync on the caller's stream.
+ *
+ * Execution: every call is asynchronous on `stream` (a cudaStream_t passed as
+ * void*; NULL is the legacy default stream) and never synchronises the host.
+ * Argument errors are returned before any launch; launch errors are returned
+ * as KMASSIGN_ERR_CUDA.  The pipeline waits inside the main kernel are
+ * bounded in time: a wait that runs out records KMASSIGN_ERR_TIMEOUT in a
+ * device status word, the kernel drains its copies, frees its tensor memory
+ * and returns; kmassign_check() reports it.  Calls on one stream are ordered;
+ * calls on different streams that write the same outputs race.
+ */
+#ifndef KMASSIGN_H
+#define KMASSIGN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum kmassign_status {
+    KMASSIGN_OK = 0,
+    KMASSIGN_ERR_NULL = -1,          /* a required pointer is NULL */
+    KMASSIGN_ERR_ALIGN = -2,         /* X or C not 16-byte aligned, or an output not 4-byte aligned */
+    KMASSIGN_ERR_SHAPE = -3,         /* N < 0, K < 1, or N or K >= 2^31 */
+    KMASSIGN_ERR_UNSUPPORTED_D = -4, /* D not a multiple of 16, or outside [16, 256] */
+    KMASSIGN_ERR_CUDA = -5,          /* a CUDA runtime/driver call failed */
+    KMASSIGN_ERR_TIMEOUT = -6,       /* a bounded wait inside a kernel ran out */
+    KMASSIGN_ERR_NOT_DEVICE = -7,    /* a pointer is not device memory */
+    KMASSIGN_ERR_ARG = -8            /* an invalid plan value in kmassign_ex */
+};
+
+/*
+ * cnorm[j] = ||c_j||^2 for j in [0, K)  (Summary: "applying centroid norms").
+ *   C      device, bf16 [K, D] row-major, 16-byte aligned
+ *   cnorm  device, fp32 [K], 4-byte aligned, written
+ * fp32 sum of the exact bf16 squares, in a fixed order (deterministic).
+ */
+int kmassign_norms(const void *C, int64_t K, int64_t D, float *cnorm, void *stream);
+
+/*
+ * idx[i] = argmin_j (||c_j||^2 - 2 x_i . c_j), lowest index on ties.
+ *   X         device, bf16 [N, D] row-major, 16-byte aligned
+ *   C         device, bf16 [K, D] row-major, 16-byte aligned
+ *   cnorm     device fp32 [K] from kmassign_norms, or NULL (then computed
+ *             inside the call into a stream-ordered temporary)
+ *   N         0 <= N < 2^31 (N == 0 launches nothing and returns OK;
+ *             X and idx may then be NULL)
+ *   K         1 <= K < 2^31
+ *   D         multiple of 16 in [16, 256]
+ *   idx       device int32 [N], written
+ *   minscore  device fp32 [N] or NULL; when given, the winning score
+ *             fmaf(-2, dot, cnorm[idx]) with -0 written as +0, or NaN for an
+ *             all-NaN row
+ * The result does not depend on how the work is tiled or split: every plan
+ * returns the same idx and minscore bits.
+ */
+int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+             int64_t D, int32_t *idx, float *minscore, void *stream);
+
+/*
+ * kmassign with an explicit plan (0 = the automatic choice for each field):
+ *   ksplit              number of centroid ranges the K axis is split into;
+ *                       > 1 merges partial winners with a 64-bit atomicMin
+ *                       on (ordered score bits << 32 | index) keys
+ *   rows_per_cta        128 or 256 points per thread block tile
+ *   centroids_per_tile  128 or 256 centroids per tensor-core tile
+ *                       (rows_per_cta 256 requires 128)
+ * Same arguments, layout and errors as kmassign; a value outside these sets
+ * returns KMASSIGN_ERR_ARG.  Tests use it to cover every path.
+ */
+int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                int64_t D, int32_t *idx, float *minscore, int ksplit, int rows_per_cta,
+                int centroids_per_tile, void *stream);
+
+/*
+ * The plan kmassign would choose for (N, K, D) on the current device:
+ * out[0] = ksplit, out[1] = rows_per_cta, out[2] = centroids_per_tile,
+ * out[3] = thread blocks launched, out[4] = shared-memory ring stages,
+ * out[5] = X tile buffers.  Launches nothing.
+ */
+int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out6);
+
+/*
+ * Synchronise `stream`, then report and clear the device status word:
+ * KMASSIGN_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * check, KMASSIGN_ERR_CUDA if the stream reports an error, else KMASSIGN_OK.
+ */
+int kmassign_check(void *stream);
+
+/* Static English text for a status code (never NULL). */
+const char *kmassign_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KMASSIGN_H */

@@ -1,0 +1,232 @@
+"""libkmassign: the k-means assignment step on one NVIDIA GB300 (sm_103a).
+
+For points X[N, D] and centroids C[K, D] (bf16), returns
+
+    idx[i] = argmin_j (||c_j||^2 - 2 x_i . c_j)      (lowest j on ties)
+
+(flashlib PR #22 "Optimize Blackwell k-means assignment reduction",
+Summary).  Every step runs in the CUDA kernels of ``libkmassign.so``; this
+module only marshals torch tensors into the C ABI declared in
+``include/kmassign.h`` and raises on error codes.  There is no CPU path: if
+the shared library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "KmassignError", "library", "library_path", "kmassign", "kmassign_ex", "kmassign_norms",
+    "kmassign_plan", "kmassign_check", "kmassign_strerror", "assign", "norms", "assign_host",
+    "STATUS",
+]
+
+STATUS = {
+    "KMASSIGN_OK": 0,
+    "KMASSIGN_ERR_NULL": -1,
+    "KMASSIGN_ERR_ALIGN": -2,
+    "KMASSIGN_ERR_SHAPE": -3,
+    "KMASSIGN_ERR_UNSUPPORTED_D": -4,
+    "KMASSIGN_ERR_CUDA": -5,
+    "KMASSIGN_ERR_TIMEOUT": -6,
+    "KMASSIGN_ERR_NOT_DEVICE": -7,
+    "KMASSIGN_ERR_ARG": -8,
+}
+_NAMES = {v: k for k, v in STATUS.items()}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KmassignError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {_NAMES.get(code, code)} ({kmassign_strerror(code)})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def _declare(lib):
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.kmassign_norms.argtypes = [vp, i64, i64, vp, vp]
+    lib.kmassign_norms.restype = i32
+    lib.kmassign.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp]
+    lib.kmassign.restype = i32
+    lib.kmassign_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, vp]
+    lib.kmassign_ex.restype = i32
+    lib.kmassign_plan.argtypes = [i64, i64, i64, vp]
+    lib.kmassign_plan.restype = i32
+    lib.kmassign_check.argtypes = [vp]
+    lib.kmassign_check.restype = i32
+    lib.kmassign_strerror.argtypes = [i32]
+    lib.kmassign_strerror.restype = ctypes.c_char_p
+    return lib
+
+
+def library(path: str | None = None):
+    """The loaded libkmassign (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or library_path()
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"libkmassign.so not found at {p}; build it with "
+                    "`python -m means_nearest_centroid_gb300._build` (there is no CPU fallback)")
+            _lib = _declare(ctypes.CDLL(p))
+        return _lib
+
+
+def kmassign_strerror(code: int) -> str:
+    return library().kmassign_strerror(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise KmassignError(code, where)
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need_cuda(t, name, dtype):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def kmassign_norms(C: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """cnorm[j] = ||c_j||^2 (fp32) on the GPU."""
+    _need_cuda(C, "C", torch.bfloat16)
+    K, D = C.shape
+    if out is None:
+        out = torch.empty(K, dtype=torch.float32, device=C.device)
+    _need_cuda(out, "out", torch.float32)
+    _check(library().kmassign_norms(_ptr(C), K, D, _ptr(out), _stream_ptr(stream)),
+           "kmassign_norms")
+    return out
+
+
+def kmassign_ex(X, C, cnorm=None, idx=None, minscore=None, ksplit: int = 0,
+                rows_per_cta: int = 0, centroids_per_tile: int = 0, stream=None):
+    """Assignment with an explicit plan (0 = automatic).  Returns idx (int32)."""
+    _need_cuda(X, "X", torch.bfloat16)
+    _need_cuda(C, "C", torch.bfloat16)
+    N, D = X.shape
+    K, D2 = C.shape
+    if D != D2:
+        raise ValueError("X and C disagree on D")
+    if cnorm is not None:
+        _need_cuda(cnorm, "cnorm", torch.float32)
+    if idx is None:
+        idx = torch.empty(N, dtype=torch.int32, device=X.device)
+    _need_cuda(idx, "idx", torch.int32)
+    if minscore is not None:
+        _need_cuda(minscore, "minscore", torch.float32)
+    rc = library().kmassign_ex(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, _ptr(idx), _ptr(minscore),
+                               int(ksplit), int(rows_per_cta), int(centroids_per_tile),
+                               _stream_ptr(stream))
+    _check(rc, "kmassign_ex")
+    return idx
+
+
+def kmassign(X, C, cnorm=None, idx=None, minscore=None, stream=None):
+    """idx[i] = argmin_j (||c_j||^2 - 2 x_i . c_j) on the GPU; returns idx."""
+    _need_cuda(X, "X", torch.bfloat16)
+    _need_cuda(C, "C", torch.bfloat16)
+    N, D = X.shape
+    K, D2 = C.shape
+    if D != D2:
+        raise ValueError("X and C disagree on D")
+    if cnorm is not None:
+        _need_cuda(cnorm, "cnorm", torch.float32)
+    if idx is None:
+        idx = torch.empty(N, dtype=torch.int32, device=X.device)
+    _need_cuda(idx, "idx", torch.int32)
+    if minscore is not None:
+        _need_cuda(minscore, "minscore", torch.float32)
+    rc = library().kmassign(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, _ptr(idx), _ptr(minscore),
+                            _stream_ptr(stream))
+    _check(rc, "kmassign")
+    return idx
+
+
+def kmassign_plan(N: int, K: int, D: int) -> dict:
+    out = (ctypes.c_int32 * 6)()
+    _check(library().kmassign_plan(int(N), int(K), int(D), ctypes.cast(out, ctypes.c_void_p)),
+           "kmassign_plan")
+    keys = ["ksplit", "rows_per_cta", "centroids_per_tile", "grid", "stages", "xbufs"]
+    return dict(zip(keys, list(out)))
+
+
+def kmassign_check(stream=None) -> int:
+    """Synchronise the stream and return the device status code (0 = OK)."""
+    return int(library().kmassign_check(_stream_ptr(stream)))
+
+
+def norms(C, stream=None):
+    return kmassign_norms(C, stream=stream)
+
+
+def assign(X, C, cnorm=None, with_minscore: bool = False, stream=None):
+    """Convenience: returns idx, or (idx, minscore) when ``with_minscore``."""
+    ms = None
+    if with_minscore:
+        ms = torch.empty(X.shape[0], dtype=torch.float32, device=X.device)
+    idx = kmassign(X, C, cnorm=cnorm, minscore=ms, stream=stream)
+    return (idx, ms) if with_minscore else idx
+
+
+def assign_host(X_host, C_host, idx_host=None, device=None, stream=None, scratch=None):
+    """End-to-end call on host tensors.
+
+    Copies X and C (ideally pinned) to the device, runs the assignment and
+    copies idx back into ``idx_host`` (pinned int32, allocated if None).
+    ``scratch`` may hold preallocated device tensors {"X", "C", "idx"} to
+    reuse.  Returns ``idx_host`` after synchronising the stream.
+    """
+    device = torch.device("cuda") if device is None else torch.device(device)
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    N = X_host.shape[0]
+    if scratch is None:
+        scratch = {}
+    with torch.cuda.stream(s):
+        Xd = scratch.get("X")
+        if Xd is None or Xd.shape != X_host.shape:
+            Xd = torch.empty(X_host.shape, dtype=X_host.dtype, device=device)
+        Cd = scratch.get("C")
+        if Cd is None or Cd.shape != C_host.shape:
+            Cd = torch.empty(C_host.shape, dtype=C_host.dtype, device=device)
+        idxd = scratch.get("idx")
+        if idxd is None or idxd.shape[0] != N:
+            idxd = torch.empty(N, dtype=torch.int32, device=device)
+        Xd.copy_(X_host, non_blocking=True)
+        Cd.copy_(C_host, non_blocking=True)
+        kmassign(Xd, Cd, idx=idxd, stream=s)
+        if idx_host is None:
+            idx_host = torch.empty(N, dtype=torch.int32, pin_memory=True)
+        idx_host.copy_(idxd, non_blocking=True)
+    s.synchronize()
+    return idx_host

@@ -1,0 +1,391 @@
+// api.cu -- the C ABI of libkmassign: argument checks, planning, temporaries,
+// TMA descriptors and launches.  No arithmetic of the method lives here.
+#include "../../include/kmassign.h"
+#include "internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+namespace {
+
+using kma::AssignParams;
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+int current_device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return KMASSIGN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return KMASSIGN_ERR_CUDA;
+        const int variants[3][2] = {{1, 128}, {1, 256}, {2, 128}};
+        for (const auto &v : variants)
+            if (kma::assign_prepare(v[0], v[1], static_cast<size_t>(d.smem_optin)) != cudaSuccess)
+                return KMASSIGN_ERR_CUDA;
+        d.ready = true;
+    }
+    *out = d;
+    return KMASSIGN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return g_encode;
+}
+
+// Row-major bf16 [rows, D], boxes of 64 columns x box_rows rows, 128-byte
+// swizzle (the K-major layout the tensor-core descriptors expect).  Boxes
+// reaching past the tensor are zero-filled by the copy engine.
+bool encode_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t D, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    cuuint64_t dims[2] = {D, rows};
+    cuuint64_t strides[1] = {D * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kma::kKBlock), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// Host or foreign pointers would make the copy engine fault: reject them.
+// Every non-NULL pointer must be device (or managed) memory of one device;
+// that device is made current for this library's runtime before launching
+// (the caller's framework may track its current device separately).
+int check_device_ptrs(const void *const *ptrs, int n)
+{
+    int owner = -1;
+    for (int i = 0; i < n; ++i) {
+        if (ptrs[i] == nullptr)
+            continue;
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, ptrs[i]) != cudaSuccess) {
+            cudaGetLastError();
+            return KMASSIGN_ERR_NOT_DEVICE;
+        }
+        if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+            return KMASSIGN_ERR_NOT_DEVICE;
+        if (a.type == cudaMemoryTypeDevice) {
+            if (owner >= 0 && a.device != owner)
+                return KMASSIGN_ERR_NOT_DEVICE;
+            owner = a.device;
+        }
+    }
+    if (owner >= 0) {
+        int cur = -1;
+        if (cudaGetDevice(&cur) != cudaSuccess)
+            return KMASSIGN_ERR_CUDA;
+        if (cur != owner && cudaSetDevice(owner) != cudaSuccess)
+            return KMASSIGN_ERR_CUDA;
+    }
+    return KMASSIGN_OK;
+}
+
+int check_shape(int64_t N, int64_t K, int64_t D)
+{
+    const int64_t lim = int64_t(1) << 31;
+    if (N < 0 || N >= lim || K < 1 || K >= lim)
+        return KMASSIGN_ERR_SHAPE;
+    if (D < 16 || D > 256 || (D % 16) != 0)
+        return KMASSIGN_ERR_UNSUPPORTED_D;
+    return KMASSIGN_OK;
+}
+
+struct Plan {
+    int sub, nt, ksplit, grid, stages, xbufs;
+    int rowtiles, ntiles, chunk_tiles, units;
+    size_t smem;
+};
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Pick tile shape and centroid split from a small cost model in SM clocks:
+// a 128x128x16 bf16 MMA takes 64 clocks; the epilogue costs about 2.5 issue
+// slots per score over 128 lanes; a unit pays ~2500 clocks to load its X tile
+// and fill the pipe; a split pays ~6000 clocks for the key memset and finalize.
+int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_ksplit,
+              int force_rows, int force_nt, Plan *out)
+{
+    const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
+    const int ksteps = static_cast<int>(D / 16);
+    const int shapes[3][2] = {{2, 128}, {1, 128}, {1, 256}};
+    bool found = false;
+    double best_cost = 0.0;
+    Plan best{};
+    for (const auto &sh : shapes) {
+        const int sub = sh[0], nt = sh[1];
+        if (force_rows != 0 && force_rows != sub * kma::kTileM)
+            continue;
+        if (force_nt != 0 && force_nt != nt)
+            continue;
+        const size_t xbytes = static_cast<size_t>(sub) * kblocks * kma::kXTileBytes;
+        const size_t stage_bytes = static_cast<size_t>(nt) * 128;
+        const size_t fixed = kma::assign_smem_bytes(sub, nt, kblocks, 0, 0);
+        const size_t budget = static_cast<size_t>(dev.smem_optin);
+        if (fixed + xbytes + 2 * stage_bytes > budget)
+            continue;
+        const int xbufs = (fixed + 2 * xbytes + 4 * stage_bytes <= budget) ? 2 : 1;
+        const int stages = static_cast<int>(std::min<size_t>(
+            kma::kMaxStages, (budget - fixed - xbufs * xbytes) / stage_bytes));
+        const int64_t ntiles = cdiv(K, nt);
+        const int64_t rowtiles = cdiv(N, static_cast<int64_t>(sub) * kma::kTileM);
+        const double tile_mma = double(sub) * (nt / 128) * ksteps * 64.0;
+        const double tile_epi = double(sub) * nt * 2.5;
+        const double tile = std::max(tile_mma, tile_epi);
+        int64_t ks_lo = 1, ks_hi = std::min<int64_t>(ntiles, 64);
+        if (force_ksplit > 0)
+            ks_lo = ks_hi = std::min<int64_t>(force_ksplit, ntiles);
+        for (int64_t ks = ks_lo; ks <= ks_hi; ++ks) {
+            const int64_t chunk = cdiv(ntiles, ks);
+            const int64_t ks_eff = cdiv(ntiles, chunk);
+            if (ks_eff != ks && force_ksplit <= 0)
+                continue;
+            const int64_t units = rowtiles * ks_eff;
+            if (units >= (int64_t(1) << 31))
+                continue;
+            const int64_t waves = cdiv(units, dev.sms);
+            const double cost = double(waves) * (double(chunk) * tile + 2500.0) +
+                                (ks_eff > 1 ? 6000.0 : 0.0);
+            if (!found || cost < best_cost * 0.999) {
+                found = true;
+                best_cost = cost;
+                best.sub = sub;
+                best.nt = nt;
+                best.ksplit = static_cast<int>(ks_eff);
+                best.rowtiles = static_cast<int>(rowtiles);
+                best.ntiles = static_cast<int>(ntiles);
+                best.chunk_tiles = static_cast<int>(chunk);
+                best.units = static_cast<int>(units);
+                best.grid = static_cast<int>(std::min<int64_t>(units, dev.sms));
+                best.stages = stages;
+                best.xbufs = xbufs;
+                best.smem = kma::assign_smem_bytes(sub, nt, kblocks, stages, xbufs);
+            }
+        }
+    }
+    if (!found)
+        return KMASSIGN_ERR_ARG;
+    *out = best;
+    return KMASSIGN_OK;
+}
+
+int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
+               int32_t *idx, float *minscore, int force_ksplit, int force_rows, int force_nt,
+               cudaStream_t stream)
+{
+    int rc = check_shape(N, K, D);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    if (force_ksplit < 0 || (force_rows != 0 && force_rows != 128 && force_rows != 256) ||
+        (force_nt != 0 && force_nt != 128 && force_nt != 256) ||
+        (force_rows == 256 && force_nt == 256))
+        return KMASSIGN_ERR_ARG;
+    if (N == 0)
+        return KMASSIGN_OK;
+    if (X == nullptr || C == nullptr || idx == nullptr)
+        return KMASSIGN_ERR_NULL;
+    if (!aligned(X, 16) || !aligned(C, 16) || (cnorm && !aligned(cnorm, 16)) || !aligned(idx, 4) ||
+        (minscore && !aligned(minscore, 4)))
+        return KMASSIGN_ERR_ALIGN;
+    const void *ptrs[5] = {X, C, cnorm, idx, minscore};
+    if ((rc = check_device_ptrs(ptrs, 5)) != KMASSIGN_OK)
+        return rc;
+
+    DeviceInfo dev;
+    if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
+        return rc;
+    Plan plan;
+    if ((rc = make_plan(N, K, D, dev, force_ksplit, force_rows, force_nt, &plan)) != KMASSIGN_OK)
+        return rc;
+
+    CUtensorMap xmap, cmap;
+    if (!encode_map(&xmap, X, static_cast<uint64_t>(N), static_cast<uint64_t>(D), kma::kTileM) ||
+        !encode_map(&cmap, C, static_cast<uint64_t>(K), static_cast<uint64_t>(D),
+                    static_cast<uint32_t>(plan.nt)))
+        return KMASSIGN_ERR_CUDA;
+
+    float *tmp_norm = nullptr;
+    unsigned long long *keys = nullptr;
+    rc = KMASSIGN_OK;
+    if (cnorm == nullptr) {
+        if (cudaMallocAsync(reinterpret_cast<void **>(&tmp_norm), static_cast<size_t>(K) * 4,
+                            stream) != cudaSuccess)
+            return KMASSIGN_ERR_CUDA;
+        if (kma::launch_norms(C, K, D, tmp_norm, stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+        cnorm = tmp_norm;
+    }
+    if (rc == KMASSIGN_OK && plan.ksplit > 1) {
+        if (cudaMallocAsync(reinterpret_cast<void **>(&keys), static_cast<size_t>(N) * 8, stream) !=
+                cudaSuccess ||
+            cudaMemsetAsync(keys, 0xff, static_cast<size_t>(N) * 8, stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+    }
+    if (rc == KMASSIGN_OK) {
+        AssignParams p{};
+        p.cnorm = cnorm;
+        p.idx = idx;
+        p.minscore = minscore;
+        p.keys = keys;
+        p.N = static_cast<int32_t>(N);
+        p.K = static_cast<int32_t>(K);
+        p.D = static_cast<int32_t>(D);
+        p.ksteps = static_cast<int32_t>(D / 16);
+        p.kblocks = static_cast<int32_t>(cdiv(D, kma::kKBlock));
+        p.rowtiles = plan.rowtiles;
+        p.ksplit = plan.ksplit;
+        p.chunk_tiles = plan.chunk_tiles;
+        p.ntiles = plan.ntiles;
+        p.num_units = plan.units;
+        p.stages = plan.stages;
+        p.xbufs = plan.xbufs;
+        p.timeout_ns = kDefaultTimeoutNs;
+        if (kma::launch_assign(plan.sub, plan.nt, p, xmap, cmap, plan.grid, plan.smem, stream) !=
+            cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+        else if (keys != nullptr && kma::launch_finalize(keys, N, idx, minscore, stream) !=
+                                        cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+    }
+    if (keys != nullptr && cudaFreeAsync(keys, stream) != cudaSuccess)
+        rc = KMASSIGN_ERR_CUDA;
+    if (tmp_norm != nullptr && cudaFreeAsync(tmp_norm, stream) != cudaSuccess)
+        rc = KMASSIGN_ERR_CUDA;
+    return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kmassign_norms(const void *C, int64_t K, int64_t D, float *cnorm, void *stream)
+{
+    int rc = check_shape(0, K, D);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    if (C == nullptr || cnorm == nullptr)
+        return KMASSIGN_ERR_NULL;
+    if (!aligned(C, 16) || !aligned(cnorm, 4))
+        return KMASSIGN_ERR_ALIGN;
+    const void *ptrs[2] = {C, cnorm};
+    if ((rc = check_device_ptrs(ptrs, 2)) != KMASSIGN_OK)
+        return rc;
+    if (kma::launch_norms(C, K, D, cnorm, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KMASSIGN_ERR_CUDA;
+    return KMASSIGN_OK;
+}
+
+int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
+             int32_t *idx, float *minscore, void *stream)
+{
+    return run_assign(X, C, cnorm, N, K, D, idx, minscore, 0, 0, 0,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
+                int32_t *idx, float *minscore, int ksplit, int rows_per_cta,
+                int centroids_per_tile, void *stream)
+{
+    return run_assign(X, C, cnorm, N, K, D, idx, minscore, ksplit, rows_per_cta,
+                      centroids_per_tile, static_cast<cudaStream_t>(stream));
+}
+
+int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out6)
+{
+    if (out6 == nullptr)
+        return KMASSIGN_ERR_NULL;
+    int rc = check_shape(N, K, D);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    DeviceInfo dev;
+    if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
+        return rc;
+    Plan plan;
+    if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, 0, 0, 0, &plan)) != KMASSIGN_OK)
+        return rc;
+    out6[0] = plan.ksplit;
+    out6[1] = plan.sub * kma::kTileM;
+    out6[2] = plan.nt;
+    out6[3] = plan.grid;
+    out6[4] = plan.stages;
+    out6[5] = plan.xbufs;
+    return KMASSIGN_OK;
+}
+
+int kmassign_check(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KMASSIGN_ERR_CUDA;
+    int code = 0;
+    if (kma::status_read_and_clear(&code) != cudaSuccess)
+        return KMASSIGN_ERR_CUDA;
+    return code;
+}
+
+const char *kmassign_strerror(int code)
+{
+    switch (code) {
+    case KMASSIGN_OK:
+        return "success";
+    case KMASSIGN_ERR_NULL:
+        return "a required pointer is NULL";
+    case KMASSIGN_ERR_ALIGN:
+        return "X and C (and cnorm) must be 16-byte aligned; idx and minscore 4-byte aligned";
+    case KMASSIGN_ERR_SHAPE:
+        return "shape out of range: need 0 <= N < 2^31 and 1 <= K < 2^31";
+    case KMASSIGN_ERR_UNSUPPORTED_D:
+        return "unsupported D: need a multiple of 16 in [16, 256]";
+    case KMASSIGN_ERR_CUDA:
+        return "a CUDA runtime or driver call failed";
+    case KMASSIGN_ERR_TIMEOUT:
+        return "a bounded pipeline wait inside a kernel ran out; the kernel drained and returned";
+    case KMASSIGN_ERR_NOT_DEVICE:
+        return "a pointer is not device memory of the current device";
+    case KMASSIGN_ERR_ARG:
+        return "invalid plan value (ksplit >= 0, rows_per_cta 128/256, centroids_per_tile "
+               "128/256, not both 256)";
+    default:
+        return "unknown kmassign status code";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// internal.h -- declarations shared by the translation units of libkmassign.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace kma {
+
+constexpr int kTileM = 128;        // points per tensor-core tile (TMEM lanes)
+constexpr int kKBlock = 64;        // bf16 elements per 128-byte swizzled row
+constexpr uint32_t kXTileBytes = kTileM * 128;  // one k-block of one 128-row X tile
+constexpr int kMaxStages = 16;     // upper bound of the shared-memory ring
+constexpr int kMaxXBufs = 2;
+constexpr int kNone = 0x7fffffff;  // "no candidate yet" index
+
+struct AssignParams {
+    const float *cnorm;            // [K] fp32
+    int32_t *idx;                  // [N] (direct store when ksplit == 1)
+    float *minscore;               // [N] or nullptr (direct store when ksplit == 1)
+    unsigned long long *keys;      // [N] packed keys (ksplit > 1), else nullptr
+    int32_t N, K, D;
+    int32_t ksteps;                // D / 16 tensor-core k-steps
+    int32_t kblocks;               // ceil(D / 64) swizzled k-blocks
+    int32_t rowtiles;              // ceil(N / (128 * sub))
+    int32_t ksplit;                // centroid ranges per row tile
+    int32_t chunk_tiles;           // centroid tiles per range
+    int32_t ntiles;                // ceil(K / nt)
+    int32_t num_units;             // rowtiles * ksplit
+    int32_t stages;                // shared-memory ring depth
+    int32_t xbufs;                 // X tile buffers (1 or 2)
+    uint64_t timeout_ns;           // bound on every pipeline wait
+};
+
+size_t assign_smem_bytes(int sub, int nt, int kblocks, int stages, int xbufs);
+cudaError_t assign_prepare(int sub, int nt, size_t smem_bytes);
+cudaError_t launch_assign(int sub, int nt, const AssignParams &p, const CUtensorMap &xmap,
+                          const CUtensorMap &cmap, int grid, size_t smem_bytes,
+                          cudaStream_t stream);
+
+cudaError_t launch_norms(const void *C, int64_t K, int64_t D, float *cnorm, cudaStream_t stream);
+cudaError_t launch_finalize(const unsigned long long *keys, int64_t N, int32_t *idx,
+                            float *minscore, cudaStream_t stream);
+
+// Read and clear the device status word (0 or a kmassign_status code).
+cudaError_t status_read_and_clear(int *code);
+
+}  // namespace kma

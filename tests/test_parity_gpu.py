@@ -1,0 +1,217 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (needs a GB300)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import means_nearest_centroid_gb300 as km
+import oracle
+import parity
+import pins
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+PLANS = [
+    dict(),                                                    # automatic
+    dict(rows_per_cta=128, centroids_per_tile=128),
+    dict(rows_per_cta=128, centroids_per_tile=256),
+    dict(rows_per_cta=256, centroids_per_tile=128),
+    dict(ksplit=3, rows_per_cta=256, centroids_per_tile=128),
+    dict(ksplit=2, rows_per_cta=128, centroids_per_tile=256),
+    dict(ksplit=5, rows_per_cta=128, centroids_per_tile=128),
+]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from means_nearest_centroid_gb300 import _build
+    _build.build()
+    km.library()
+    return torch.device("cuda:0")
+
+
+def run(dev, X, C, cnorm=None, with_cnorm=False, plan=None, minscore=True):
+    Xd, Cd = X.to(dev), C.to(dev)
+    cn = None
+    if with_cnorm:
+        cn = km.kmassign_norms(Cd)
+    if cnorm is not None:
+        cn = cnorm
+    ms = torch.full((X.shape[0],), 12345.0, dtype=torch.float32, device=dev) if minscore else None
+    idx = torch.full((X.shape[0],), -7, dtype=torch.int32, device=dev)
+    if plan:
+        km.kmassign_ex(Xd, Cd, cnorm=cn, idx=idx, minscore=ms, **plan)
+    else:
+        km.kmassign(Xd, Cd, cnorm=cn, idx=idx, minscore=ms)
+    assert km.kmassign_check() == 0
+    return idx.cpu(), (ms.cpu() if ms is not None else None)
+
+
+def pad_d(t, D=16):
+    out = torch.zeros(t.shape[0], D, dtype=torch.bfloat16)
+    out[:, :t.shape[1]] = t
+    return out
+
+
+# ---------------------------------------------------------------- norms
+@pytest.mark.parametrize("K,D", [(1, 16), (7, 64), (1000, 128), (4099, 256), (300, 48)])
+def test_norms_match_oracle(dev, K, D):
+    _, C = workloads.iid(1, K, D, seed=K + D)
+    got = km.kmassign_norms(C.to(dev)).cpu().double().numpy()
+    ref = oracle.norms(C)
+    # sum of positive terms: relative error <= (D - 1) * 2^-24
+    assert np.all(np.abs(got - ref) <= D * 2.0**-24 * ref + 1e-30)
+    _, Ci = workloads.integers(1, K, D, seed=K * D)
+    assert np.array_equal(km.kmassign_norms(Ci.to(dev)).cpu().double().numpy(), oracle.norms(Ci))
+
+
+# ---------------------------------------------------------------- hand cases
+@pytest.mark.parametrize("plan", PLANS[:4], ids=str)
+def test_golden_cases(dev, plan):
+    for case in pins.load_golden():
+        X = pad_d(pins._bf16_rows(case["X"]))
+        C = pad_d(pins._bf16_rows(case["C"]))
+        idx, ms = run(dev, X, C, plan=plan)
+        assert idx.tolist() == case["idx"], case["name"]
+        for got, exp in zip(ms.tolist(), case["minscore"]):
+            assert pins._same_score(got, pins._val(exp)), (case["name"], got, exp)
+
+
+# ---------------------------------------------------------------- small shapes
+SHAPES = [(1, 1, 16), (1, 3, 64), (5, 7, 32), (300, 130, 64), (129, 257, 256),
+          (1000, 777, 128), (2000, 1000, 48), (4096, 128, 64), (333, 2049, 96)]
+
+
+@pytest.mark.parametrize("N,K,D", SHAPES)
+@pytest.mark.parametrize("pi", range(len(PLANS)))
+def test_float_shapes_all_plans(dev, N, K, D, pi):
+    X, C = workloads.blobs(N, K, D, seed=N * 7 + K * 3 + D)
+    idx, ms = run(dev, X, C, plan=PLANS[pi], with_cnorm=(pi % 2 == 1))
+    rep = parity.compare(X, C, idx, ms)
+    assert rep.ok(), rep
+
+
+@pytest.mark.parametrize("N,K,D", SHAPES)
+def test_integer_shapes_bit_exact(dev, N, K, D):
+    X, C = workloads.integers(N, K, D, seed=N + K + D)
+    results = []
+    for plan in PLANS:
+        idx, ms = run(dev, X, C, plan=plan)
+        rep = parity.compare(X, C, idx, ms, integer=True)
+        assert rep.ok() and rep.idx_mismatches == 0, (plan, rep)
+        results.append((idx, ms))
+    for idx, ms in results[1:]:
+        assert torch.equal(idx, results[0][0])
+        assert torch.equal(ms.view(torch.int32), results[0][1].view(torch.int32))
+
+
+def test_adversarial_reduced_bit_exact(dev):
+    X, C = workloads.adversarial(6000, 2048, 64, seed=44)
+    for plan in PLANS:
+        idx, ms = run(dev, X, C, plan=plan)
+        rep = parity.compare(X, C, idx, ms, integer=True)
+        assert rep.ok() and rep.idx_mismatches == 0, (plan, rep)
+
+
+def test_plans_give_identical_bits_on_float_data(dev):
+    X, C = workloads.iid(1500, 1300, 128, seed=99)
+    ref = None
+    for plan in PLANS:
+        idx, ms = run(dev, X, C, plan=plan)
+        if ref is None:
+            ref = (idx, ms)
+            continue
+        assert torch.equal(idx, ref[0]), plan
+        assert torch.equal(ms.view(torch.int32), ref[1].view(torch.int32)), plan
+
+
+def test_repeat_runs_are_bitwise_identical(dev):
+    X, C = workloads.iid(3000, 2500, 64, seed=3)
+    Xd, Cd = X.to(dev), C.to(dev)
+    first = km.kmassign(Xd, Cd).clone()
+    for _ in range(20):
+        assert torch.equal(km.kmassign(Xd, Cd), first)
+
+
+def test_minscore_optional_and_idx_only(dev):
+    X, C = workloads.blobs(700, 300, 64, seed=8)
+    idx_a, _ = run(dev, X, C, minscore=False)
+    idx_b, _ = run(dev, X, C, minscore=True)
+    assert torch.equal(idx_a, idx_b)
+
+
+def test_empty_input(dev):
+    X = torch.empty(0, 64, dtype=torch.bfloat16, device=dev)
+    C = torch.ones(4, 64, dtype=torch.bfloat16, device=dev)
+    idx = km.kmassign(X, C)
+    assert idx.numel() == 0
+
+
+def test_host_pointer_rejected(dev):
+    X, C = workloads.iid(10, 4, 64, seed=1)
+    lib = km.library()
+    idx = torch.empty(10, dtype=torch.int32, device=dev)
+    rc = lib.kmassign(km._ptr(X), km._ptr(C.to(dev)), km._ptr(None), 10, 4, 64, km._ptr(idx),
+                      km._ptr(None), km._stream_ptr(None))
+    assert rc == km.STATUS["KMASSIGN_ERR_NOT_DEVICE"]
+
+
+def test_assign_host_end_to_end(dev):
+    X, C = workloads.blobs(1000, 200, 128, seed=12)
+    got = km.assign_host(X.pin_memory(), C.pin_memory())
+    rep = parity.compare(X, C, got, None)
+    assert rep.ok(), rep
+
+
+def test_non_default_stream(dev):
+    X, C = workloads.blobs(2000, 600, 64, seed=13)
+    s = torch.cuda.Stream()
+    Xd, Cd = X.to(dev), C.to(dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        idx = km.kmassign(Xd, Cd, stream=s)
+    s.synchronize()
+    rep = parity.compare(X, C, idx.cpu(), None)
+    assert rep.ok(), rep
+
+
+# ---------------------------------------------------------------- full sizes
+FULL_SAMPLE = {"tiny_blobs": None, "sampled_centroids": 8192, "iid_normal": 2048,
+               "lognormal_clusters": 4096, "adversarial_ties": None}
+
+
+@pytest.mark.parametrize("key", workloads.ORDER)
+def test_full_size_workloads(dev, key):
+    w = workloads.WORKLOADS[key]
+    X, C = workloads.make(key)
+    Xd, Cd = X.to(dev), C.to(dev)
+    cn = km.kmassign_norms(Cd) if w.precomputed_norms else None
+    ms = torch.empty(w.N, dtype=torch.float32, device=dev)
+    idx = km.kmassign(Xd, Cd, cnorm=cn, minscore=ms)
+    assert km.kmassign_check() == 0
+    idx, ms = idx.cpu(), ms.cpu()
+    n = FULL_SAMPLE[key]
+    if n is None:
+        rows = None
+    else:
+        g = np.random.default_rng(w.seed)
+        rows = np.unique(np.concatenate([g.choice(w.N, n, replace=False),
+                                         [0, w.N - 1], np.arange(w.N - 300, w.N)]))
+    rep = parity.compare(X, C, idx, ms, rows=rows, integer=w.integer)
+    print(key, rep)
+    assert rep.ok(), rep
+    if w.integer:
+        assert rep.idx_mismatches == 0
+    # properties that hold on every row at any size
+    assert int(idx.min()) >= 0 and int(idx.max()) < w.K
+    if w.key == "adversarial_ties":
+        # twins: the lower copy always wins over its duplicate at j + K/2
+        finite = torch.isfinite(ms)
+        assert bool((idx[finite] < w.K // 2).all())
+        nan_rows = torch.isnan(X.float()).any(1)
+        assert bool((idx[nan_rows] == 0).all()) and bool(torch.isnan(ms[nan_rows]).all())
