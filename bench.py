@@ -173,10 +173,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside), "window": window}
 
 
-def make_inputs(key, variants, device):
+def make_inputs(key, variants, device, N=None, K=None, D=None):
     sets = []
     for v in range(variants):
-        X, C = workloads.make(key, variant=v)
+        X, C = workloads.make(key, N=N, K=K, D=D, variant=v)
         sets.append((X, C))
     dev_sets = [(X.to(device), C.to(device)) for X, C in sets]
     return sets, dev_sets
@@ -263,6 +263,9 @@ def main():
     ap.add_argument("--ref-budget-s", type=float, default=150.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--parity-rows", type=int, default=256)
+    ap.add_argument("--N", type=int, default=None, help="override the workload's N")
+    ap.add_argument("--K", type=int, default=None, help="override the workload's K")
+    ap.add_argument("--D", type=int, default=None, help="override the workload's D")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -290,9 +293,12 @@ def main():
     km.library()
 
     w = workloads.WORKLOADS[key]
-    N, D, K = w.N, w.D, w.K
+    N = w.N if args.N is None else args.N
+    D = w.D if args.D is None else args.D
+    K = w.K if args.K is None else args.K
+    resized = (N, D, K) != (w.N, w.D, w.K)
     flops = 2.0 * N * K * D
-    sets, dsets = make_inputs(key, 3, device)
+    sets, dsets = make_inputs(key, 3, device, N, K, D)
     cns = [torch.empty(K, dtype=torch.float32, device=device) for _ in dsets]
     idxs = [torch.empty(N, dtype=torch.int32, device=device) for _ in dsets]
     stream = torch.cuda.current_stream(device)
@@ -430,9 +436,11 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak",
-        "vs_baseline": (value / PAGES_B200_TFLOPS[key]) if key in PAGES_B200_TFLOPS else None,
+        "vs_baseline": (value / PAGES_B200_TFLOPS[key])
+        if (key in PAGES_B200_TFLOPS and not resized) else None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.text, "key": key, "N": N, "D": D, "K": K,
+        "config": {"workload": (f"{key} distribution resized to N={N}, D={D}, K={K}"
+                                if resized else w.text), "key": key, "N": N, "D": D, "K": K,
                    "norms_in_step": norms_in_step,
                    "l2": "3 rotating seeded input sets per GPU, larger than the 126 MB L2 "
                          "together",

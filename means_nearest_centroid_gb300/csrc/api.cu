@@ -1,6 +1,6 @@
 // api.cu -- the C ABI of libkmassign: argument checks, planning, temporaries,
 // TMA descriptors and launches.  No arithmetic of the method lives here.
-#include "../../include/kmassign.h"
+#include "kmassign.h"
 #include "internal.h"
 
 #include <cudaTypedefs.h>
@@ -39,10 +39,10 @@ int current_device_info(DeviceInfo *out)
             cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
                 cudaSuccess)
             return KMASSIGN_ERR_CUDA;
-        const int variants[3][2] = {{1, 128}, {1, 256}, {2, 128}};
-        for (const auto &v : variants)
-            if (kma::assign_prepare(v[0], v[1], static_cast<size_t>(d.smem_optin)) != cudaSuccess)
-                return KMASSIGN_ERR_CUDA;
+        for (const auto &v : kma::kVariants)
+            for (int kb = 1; kb <= 4; ++kb)
+                if (kma::assign_prepare(v, kb, static_cast<size_t>(d.smem_optin)) != cudaSuccess)
+                    return KMASSIGN_ERR_CUDA;
         d.ready = true;
     }
     *out = d;
@@ -131,45 +131,50 @@ int check_shape(int64_t N, int64_t K, int64_t D)
 }
 
 struct Plan {
-    int sub, nt, ksplit, grid, stages, xbufs;
+    kma::Variant v;
+    int ksplit, grid, stages, xbufs;
     int rowtiles, ntiles, chunk_tiles, units;
     size_t smem;
 };
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Pick tile shape and centroid split from a small cost model in SM clocks:
-// a 128x128x16 bf16 MMA takes 64 clocks; the epilogue costs about 2.5 issue
-// slots per score over 128 lanes; a unit pays ~2500 clocks to load its X tile
-// and fill the pipe; a split pays ~6000 clocks for the key memset and finalize.
+// Pick the kernel shape and the centroid split from a cost model in SM
+// clocks per centroid tile, fitted to measurements of the kernel on GB300:
+//   * tensor pipe: a 128x256x16 bf16 MMA takes 128 clocks back to back, a
+//     128x128x16 one ~80 with two accumulators and ~92 with one, plus a
+//     per-tile hand-over cost;
+//   * epilogue: the consumer warps need ~3000 clocks per 128x256 tile with 8
+//     warps, ~2500 per 256x128 tile with 8 warps, ~2000 per 128x128 tile
+//     with 4 warps (latency-bound; measured on iid and clustered data);
+//   * a unit pays ~2500 clocks to load its X tile and fill the pipe; a split
+//     pays ~6000 clocks for the key memset and the finalize kernel.
 int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_ksplit,
               int force_rows, int force_nt, Plan *out)
 {
     const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
-    const int ksteps = static_cast<int>(D / 16);
-    const int shapes[3][2] = {{2, 128}, {1, 128}, {1, 256}};
     bool found = false;
     double best_cost = 0.0;
     Plan best{};
-    for (const auto &sh : shapes) {
-        const int sub = sh[0], nt = sh[1];
-        if (force_rows != 0 && force_rows != sub * kma::kTileM)
+    for (const auto &v : kma::kVariants) {
+        if (force_rows != 0 && force_rows != v.sub * kma::kTileM)
             continue;
-        if (force_nt != 0 && force_nt != nt)
+        if (force_nt != 0 && force_nt != v.nt)
             continue;
-        const size_t xbytes = static_cast<size_t>(sub) * kblocks * kma::kXTileBytes;
-        const size_t stage_bytes = static_cast<size_t>(nt) * 128;
-        const size_t fixed = kma::assign_smem_bytes(sub, nt, kblocks, 0, 0);
+        const size_t xbytes = static_cast<size_t>(v.sub) * kblocks * kma::kXTileBytes;
+        const size_t stage_bytes = static_cast<size_t>(v.nt) * 128;
+        const size_t fixed = kma::assign_smem_bytes(v, kblocks, 0, 0);
         const size_t budget = static_cast<size_t>(dev.smem_optin);
         if (fixed + xbytes + 2 * stage_bytes > budget)
             continue;
         const int xbufs = (fixed + 2 * xbytes + 4 * stage_bytes <= budget) ? 2 : 1;
         const int stages = static_cast<int>(std::min<size_t>(
             kma::kMaxStages, (budget - fixed - xbufs * xbytes) / stage_bytes));
-        const int64_t ntiles = cdiv(K, nt);
-        const int64_t rowtiles = cdiv(N, static_cast<int64_t>(sub) * kma::kTileM);
-        const double tile_mma = double(sub) * (nt / 128) * ksteps * 64.0;
-        const double tile_epi = double(sub) * nt * 2.5;
+        const int64_t ntiles = cdiv(K, v.nt);
+        const int64_t rowtiles = cdiv(N, static_cast<int64_t>(v.sub) * kma::kTileM);
+        const double mma_clk = v.nt == 256 ? 128.0 : (v.sub == 2 ? 80.0 : 92.0);
+        const double tile_mma = double(v.sub) * kblocks * 4 * mma_clk + (v.nt == 256 ? 700 : 500);
+        const double tile_epi = v.nt == 256 ? 3000.0 : (v.sub == 2 ? 2480.0 : 2000.0);
         const double tile = std::max(tile_mma, tile_epi);
         int64_t ks_lo = 1, ks_hi = std::min<int64_t>(ntiles, 64);
         if (force_ksplit > 0)
@@ -185,11 +190,10 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
             const int64_t waves = cdiv(units, dev.sms);
             const double cost = double(waves) * (double(chunk) * tile + 2500.0) +
                                 (ks_eff > 1 ? 6000.0 : 0.0);
-            if (!found || cost < best_cost * 0.999) {
+            if (!found || cost < best_cost * 0.98) {
                 found = true;
                 best_cost = cost;
-                best.sub = sub;
-                best.nt = nt;
+                best.v = v;
                 best.ksplit = static_cast<int>(ks_eff);
                 best.rowtiles = static_cast<int>(rowtiles);
                 best.ntiles = static_cast<int>(ntiles);
@@ -198,7 +202,7 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
                 best.grid = static_cast<int>(std::min<int64_t>(units, dev.sms));
                 best.stages = stages;
                 best.xbufs = xbufs;
-                best.smem = kma::assign_smem_bytes(sub, nt, kblocks, stages, xbufs);
+                best.smem = kma::assign_smem_bytes(v, kblocks, stages, xbufs);
             }
         }
     }
@@ -240,7 +244,7 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
     CUtensorMap xmap, cmap;
     if (!encode_map(&xmap, X, static_cast<uint64_t>(N), static_cast<uint64_t>(D), kma::kTileM) ||
         !encode_map(&cmap, C, static_cast<uint64_t>(K), static_cast<uint64_t>(D),
-                    static_cast<uint32_t>(plan.nt)))
+                    static_cast<uint32_t>(plan.v.nt)))
         return KMASSIGN_ERR_CUDA;
 
     float *tmp_norm = nullptr;
@@ -279,7 +283,7 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
         p.stages = plan.stages;
         p.xbufs = plan.xbufs;
         p.timeout_ns = kDefaultTimeoutNs;
-        if (kma::launch_assign(plan.sub, plan.nt, p, xmap, cmap, plan.grid, plan.smem, stream) !=
+        if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, plan.grid, plan.smem, stream) !=
             cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
         else if (keys != nullptr && kma::launch_finalize(keys, N, idx, minscore, stream) !=
@@ -343,8 +347,8 @@ int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out6)
     if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, 0, 0, 0, &plan)) != KMASSIGN_OK)
         return rc;
     out6[0] = plan.ksplit;
-    out6[1] = plan.sub * kma::kTileM;
-    out6[2] = plan.nt;
+    out6[1] = plan.v.sub * kma::kTileM;
+    out6[2] = plan.v.nt;
     out6[3] = plan.grid;
     out6[4] = plan.stages;
     out6[5] = plan.xbufs;

@@ -11,19 +11,31 @@
 //                      tile stays resident while centroids stream past it)
 //                      and streams C k-blocks through a ring of shared-memory
 //                      stages guarded by full/empty mbarriers;
-//   * MMA warp       - one thread issues tcgen05.mma (bf16 in, fp32 out) into
-//                      one of two tensor-memory accumulator stages and
-//                      commits completion to mbarriers;
-//   * consumer warps - 4 per 128-point sub-tile, one point per thread: load
-//                      the scores with tcgen05.ld, wait for the loads, hand
-//                      the accumulator stage back (the fenced-load pattern of
-//                      the Key ideas table), then apply the norms and reduce.
+//   * MMA warp       - converged, one elected lane issues tcgen05.mma (bf16
+//                      in, fp32 out) into one of two tensor-memory accumulator
+//                      stages; the k-loop is unrolled at compile time with the
+//                      operand descriptors computed once per unit, because the
+//                      tensor pipe's issue queue is shallow and any extra work
+//                      between MMAs shows up as pipe bubbles;
+//   * consumer warps - 4 per 128-point sub-tile and column slice, one point
+//                      per thread: load the scores with tcgen05.ld, wait for
+//                      the loads, hand the accumulator stage back (the
+//                      fenced-load pattern of the Key ideas table), then apply
+//                      the norms and reduce.
+//
+// Centroid norms reach the consumers through shared memory: the consumer
+// threads fetch the next tile's norms from global memory while the current
+// tile is reduced and publish them behind a named barrier, so the reduction
+// reads them with broadcast shared loads (the L1 cache is mostly carved out
+// for the operand ring and would miss).
 //
 // The reduction works on 32-column chunks: s = fmaf(-2, acc, cnorm) for the
 // chunk (two lanes per packed fma), the chunk minimum by a 3-input min tree
-// (NaN ignored), and only when that minimum beats the running best the first
-// column holding it is searched.  Scanning chunks in increasing centroid
-// order keeps the lowest index on ties; a NaN score never wins.
+// (NaN ignored) -- four chunks at a time so their dependency chains overlap --
+// and only when a chunk minimum beats the running best is the first column
+// holding it searched.  Chunks are visited in increasing centroid order, so a
+// warp keeps the lowest index on ties; column slices and split centroid
+// ranges merge by (score, index).  A NaN score never wins.
 //
 // A work unit is (row tile, centroid range).  When the centroid axis is
 // split, partial winners meet in a 64-bit atomicMin on keys holding the
@@ -32,13 +44,14 @@
 //
 // Every mbarrier wait is bounded by p.timeout_ns of %globaltimer.  A wait that
 // runs out records KMASSIGN_ERR_TIMEOUT in the status word and raises a
-// block-wide abort flag; all roles then leave their loops, the producer waits
-// (again bounded) for its copies in flight, the MMA thread waits for its MMAs,
-// and the tensor memory is freed before the block returns.
+// block-wide abort flag; after that every wait returns at once, consumer
+// warps skip their work but keep meeting their named barriers, the producer
+// waits (again bounded) for its copies in flight, the MMA warp waits for its
+// MMAs, and the tensor memory is freed before the block returns.
 #include "internal.h"
 #include "ptx.cuh"
 
-#include "../../include/kmassign.h"
+#include "kmassign.h"
 
 namespace kma {
 
@@ -46,28 +59,27 @@ __device__ int g_status_word = 0;
 
 namespace {
 
-// Barrier slots (8 bytes each) after the operand buffers.
-constexpr int kBarXFull = 0;                       // [kMaxXBufs]
-constexpr int kBarXEmpty = kBarXFull + kMaxXBufs;  // [kMaxXBufs]
+// Barrier slots (8 bytes each) after the operand and staging buffers.
+constexpr int kBarXFull = 0;                          // [kMaxXBufs]
+constexpr int kBarXEmpty = kBarXFull + kMaxXBufs;     // [kMaxXBufs]
 constexpr int kBarAccFull = kBarXEmpty + kMaxXBufs;   // [2]
 constexpr int kBarAccEmpty = kBarAccFull + 2;         // [2]
 constexpr int kBarDrain = kBarAccEmpty + 2;           // [1]
 constexpr int kBarCFull = kBarDrain + 1;              // [kMaxStages]
 constexpr int kBarCEmpty = kBarCFull + kMaxStages;    // [kMaxStages]
 constexpr int kNumBars = kBarCEmpty + kMaxStages;
-constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;   // + tmem slot + abort flag
+constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot + abort flag
+constexpr uint32_t kConsumerBarrier = 1;              // named barrier id
 
 __device__ __forceinline__ void record_timeout()
 {
     atomicCAS(&g_status_word, 0, static_cast<int>(KMASSIGN_ERR_TIMEOUT));
 }
 
-// Single-thread bounded wait.  Returns false on timeout or block abort.
-__device__ __noinline__ bool wait1(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                   uint64_t limit_ns, bool honour_abort)
+// Slow path of a bounded wait (the phase was not complete on first try).
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                       uint64_t limit_ns, bool honour_abort)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity))
@@ -82,27 +94,31 @@ __device__ __noinline__ bool wait1(uint32_t bar, uint32_t parity, volatile uint3
     }
 }
 
+// Single-thread bounded wait.  Returns false on timeout or block abort.
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                      uint64_t limit_ns, bool honour_abort = true)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    return wait_slow(bar, parity, abort_flag, limit_ns, honour_abort);
+}
+
 // Whole-warp bounded wait; the decision is uniform across the warp.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
                                           volatile uint32_t *abort_flag, uint64_t limit_ns,
-                                          int lane)
+                                          bool honour_abort = true)
 {
-    uint64_t t0 = 0;
-    bool started = false;
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
     while (true) {
-        const bool done = mbar_try_wait(bar, parity);
-        if (__all_sync(0xffffffffu, done))
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
             return true;
         int give_up = 0;
-        if (lane == 0) {
-            const uint64_t now = globaltimer_ns();
-            if (!started) {
-                t0 = now;
-                started = true;
-            }
-            if (*abort_flag) {
+        if ((threadIdx.x & 31) == 0) {
+            if (honour_abort && *abort_flag) {
                 give_up = 1;
-            } else if (now - t0 > limit_ns) {
+            } else if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1u;
                 record_timeout();
                 give_up = 1;
@@ -145,31 +161,8 @@ __device__ __forceinline__ unsigned long long pack_key(float s, int j)
     return (static_cast<unsigned long long>(o) << 32) | static_cast<uint32_t>(j);
 }
 
-// One 32-column chunk of one point's scores: fold into (best, bi).
-__device__ __forceinline__ void reduce_chunk(const float (&acc)[32], const AssignParams &p, int j0,
-                                             float &best, int &bi)
+__device__ __forceinline__ float chunk_min(const float (&s)[32])
 {
-    float cn[32];
-    if (j0 + 32 <= p.K) {
-        const float4 *src = reinterpret_cast<const float4 *>(p.cnorm + j0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 q = __ldg(src + i);
-            cn[4 * i + 0] = q.x;
-            cn[4 * i + 1] = q.y;
-            cn[4 * i + 2] = q.z;
-            cn[4 * i + 3] = q.w;
-        }
-    } else {
-        // columns past K: a NaN norm makes a NaN score, which never wins
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            cn[i] = (j0 + i < p.K) ? __ldg(p.cnorm + j0 + i) : __int_as_float(0x7fc00000);
-    }
-    float s[32];
-#pragma unroll
-    for (int i = 0; i < 32; i += 2)
-        fma2(s[i], s[i + 1], -2.0f, -2.0f, acc[i], acc[i + 1], cn[i], cn[i + 1]);
     float a[11];
 #pragma unroll
     for (int i = 0; i < 10; ++i)
@@ -179,7 +172,24 @@ __device__ __forceinline__ void reduce_chunk(const float (&acc)[32], const Assig
     const float b1 = min3(a[3], a[4], a[5]);
     const float b2 = min3(a[6], a[7], a[8]);
     const float b3 = min2(a[9], a[10]);
-    const float m = min3(b0, b1, min2(b2, b3));
+    return min3(b0, b1, min2(b2, b3));
+}
+
+// s[i] = fmaf(-2, acc[i], cnorm[j0 + i]) in place, norms from shared memory.
+__device__ __forceinline__ void apply_norms(float (&v)[32], uint32_t cn_addr)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 c = ld_shared_v4(cn_addr + 16u * i);
+        fma2(v[4 * i + 0], v[4 * i + 1], -2.0f, -2.0f, v[4 * i + 0], v[4 * i + 1], c.x, c.y);
+        fma2(v[4 * i + 2], v[4 * i + 3], -2.0f, -2.0f, v[4 * i + 2], v[4 * i + 3], c.z, c.w);
+    }
+}
+
+// Fold chunk scores s (columns j0 .. j0+31, chunk minimum m) into (best, bi).
+__device__ __forceinline__ void fold_chunk(const float (&s)[32], float m, int j0, float &best,
+                                           int &bi)
+{
     if (m < best || (m == best && bi == kNone)) {
         int pos = 31;
 #pragma unroll
@@ -190,28 +200,37 @@ __device__ __forceinline__ void reduce_chunk(const float (&acc)[32], const Assig
     }
 }
 
-template <int SUB, int NT>
-__global__ void __launch_bounds__(32 * (4 * SUB + 2), 1)
+template <int SUB, int NT, int CH, int KB>
+__global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
     assign_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap cmap,
                   const AssignParams p)
 {
-    constexpr int kConsumerWarps = 4 * SUB;
+    constexpr int kConsumerWarps = 4 * SUB * CH;
+    constexpr int kConsumerThreads = 32 * kConsumerWarps;
     constexpr int kProducerWarp = kConsumerWarps;
     constexpr int kMmaWarp = kConsumerWarps + 1;
+    constexpr int kCW = NT / CH;                       // columns per consumer warp per tile
+    constexpr int kChunks = kCW / 32;
+    constexpr int kGroup = kChunks < 4 ? kChunks : 4;  // chunks loaded per tcgen05.wait::ld
+    constexpr int kGroups = kChunks / kGroup;
     constexpr uint32_t kCStageBytes = NT * 128;
-    constexpr uint32_t kAccCols = SUB * NT;        // columns of one accumulator stage
-    constexpr uint32_t kTmemCols = 2 * kAccCols;   // two stages: 256 or 512
+    constexpr uint32_t kXBufBytes = SUB * KB * kXTileBytes;
+    constexpr uint32_t kAccCols = SUB * NT;            // columns of one accumulator stage
+    constexpr uint32_t kTmemCols = 2 * kAccCols;       // two stages: 256 or 512
     constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, NT);
+    constexpr int kNormPerThread = (NT + kConsumerThreads - 1) / kConsumerThreads;
     static_assert(kTmemCols <= 512, "accumulators exceed tensor memory");
-    static_assert(NT % 128 == 0, "consumer groups read 128 columns at a time");
+    static_assert(kCW % 32 == 0 && kChunks % kGroup == 0, "column slice must be whole chunks");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t x_buf_bytes = SUB * p.kblocks * kXTileBytes;
     const uint32_t x_base = base;
-    const uint32_t c_base = x_base + p.xbufs * x_buf_bytes;
-    const uint32_t bar_base = c_base + p.stages * kCStageBytes;
+    const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
+    const uint32_t cn_base = c_base + p.stages * kCStageBytes;       // float[2][NT]
+    const uint32_t red_base = cn_base + 2 * NT * 4;                   // {float,int}[CH-1][SUB*128]
+    const uint32_t bar_base = red_base + (CH - 1) * SUB * kTileM * 8;
+    uint8_t *const sbase = smem_raw + (base - raw);
     uint8_t *misc_ptr = smem_raw + (bar_base - raw) + kNumBars * 8;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(misc_ptr);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(misc_ptr + 4);
@@ -259,19 +278,21 @@ __global__ void __launch_bounds__(32 * (4 * SUB + 2), 1)
                 const Unit w = decode_unit<SUB>(p, u);
                 const uint32_t xb = x_issued % p.xbufs;
                 const uint32_t xph = (x_issued / p.xbufs) & 1u;
-                if (!(ok = wait1(bar(kBarXEmpty + xb), xph ^ 1u, abort_flag, p.timeout_ns, true)))
+                if (!(ok = wait1(bar(kBarXEmpty + xb), xph ^ 1u, abort_flag, p.timeout_ns)))
                     break;
-                mbar_arrive_expect_tx(bar(kBarXFull + xb), w.nsub * p.kblocks * kXTileBytes);
-                const uint32_t xdst = x_base + xb * x_buf_bytes;
+                mbar_arrive_expect_tx(bar(kBarXFull + xb), w.nsub * KB * kXTileBytes);
+                const uint32_t xdst = x_base + xb * kXBufBytes;
                 for (int t = 0; t < w.nsub; ++t)
-                    for (int kb = 0; kb < p.kblocks; ++kb)
-                        tma_load_2d(xdst + (t * p.kblocks + kb) * kXTileBytes, &xmap,
-                                    bar(kBarXFull + xb), kb * kKBlock, w.row0 + t * kTileM, pol_x);
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_load_2d(xdst + (t * KB + kb) * kXTileBytes, &xmap, bar(kBarXFull + xb),
+                                    kb * kKBlock, w.row0 + t * kTileM, pol_x);
                 ++x_issued;
                 for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
-                    for (int kb = 0; kb < p.kblocks; ++kb) {
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) {
                         if (!(ok = wait1(bar(kBarCEmpty + stage), phase ^ 1u, abort_flag,
-                                         p.timeout_ns, true)))
+                                         p.timeout_ns)))
                             break;
                         mbar_arrive_expect_tx(bar(kBarCFull + stage), kCStageBytes);
                         tma_load_2d(c_base + stage * kCStageBytes, &cmap, bar(kBarCFull + stage),
@@ -296,115 +317,197 @@ __global__ void __launch_bounds__(32 * (4 * SUB + 2), 1)
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0;
-            bool ok = true, issued = false;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const Unit w = decode_unit<SUB>(p, u);
-                const uint32_t xb = x_used % p.xbufs;
-                const uint32_t xph = (x_used / p.xbufs) & 1u;
-                if (!(ok = wait1(bar(kBarXFull + xb), xph, abort_flag, p.timeout_ns, true)))
+        // The whole warp walks the schedule and waits; one elected lane issues.
+        uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0;
+        bool ok = true, issued = false;
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const Unit w = decode_unit<SUB>(p, u);
+            const uint32_t xb = x_used % p.xbufs;
+            const uint32_t xph = (x_used / p.xbufs) & 1u;
+            // Operands landed by TMA are ordered by the mbarrier itself; no
+            // tcgen05 fence is needed before MMAs read them.
+            if (!(ok = wait_warp(bar(kBarXFull + xb), xph, abort_flag, p.timeout_ns)))
+                break;
+            uint64_t adesc[SUB][KB];
+#pragma unroll
+            for (int t = 0; t < SUB; ++t)
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+                    adesc[t][kb] = sw128_kmajor_desc(x_base + xb * kXBufBytes +
+                                                     (t * KB + kb) * kXTileBytes);
+            for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
+                const uint32_t as = acc_used & 1u;
+                const uint32_t aph = (acc_used >> 1) & 1u;
+                if (!(ok = wait_warp(bar(kBarAccEmpty + as), aph ^ 1u, abort_flag, p.timeout_ns)))
                     break;
                 tc_fence_after();
-                const uint32_t xsrc = x_base + xb * x_buf_bytes;
-                for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
-                    const uint32_t as = acc_used & 1u;
-                    const uint32_t aph = (acc_used >> 1) & 1u;
-                    if (!(ok = wait1(bar(kBarAccEmpty + as), aph ^ 1u, abort_flag, p.timeout_ns, true)))
+                const uint32_t d_tmem = tmem_base + as * kAccCols;
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!(ok = wait_warp(bar(kBarCFull + stage), phase, abort_flag, p.timeout_ns)))
                         break;
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + as * kAccCols;
-                    for (int kb = 0; kb < p.kblocks; ++kb) {
-                        if (!(ok = wait1(bar(kBarCFull + stage), phase, abort_flag, p.timeout_ns,
-                                         true)))
-                            break;
-                        tc_fence_after();
-                        const uint64_t cdesc = sw128_kmajor_desc(c_base + stage * kCStageBytes);
-                        const int kk = min(4, p.ksteps - kb * 4);
-                        for (int k = 0; k < kk; ++k) {
-                            for (int t = 0; t < w.nsub; ++t) {
-                                const uint64_t adesc =
-                                    sw128_kmajor_desc(xsrc + (t * p.kblocks + kb) * kXTileBytes);
-                                mma_bf16(d_tmem + t * NT, adesc + 2u * k, cdesc + 2u * k, kIdesc,
-                                         (kb | k) != 0);
-                            }
-                        }
-                        issued = true;
+                    const uint64_t cdesc = sw128_kmajor_desc(c_base + stage * kCStageBytes);
+                    if (elect_one()) {
+                        // Sub-tiles past the last point compute on stale
+                        // operands; their rows are never stored.
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+#pragma unroll
+                            for (int t = 0; t < SUB; ++t)
+                                mma_bf16(d_tmem + t * NT, adesc[t][kb] + 2u * k, cdesc + 2u * k,
+                                         kIdesc, (kb | k) != 0);
                         mma_commit(bar(kBarCEmpty + stage));
-                        if (++stage == static_cast<uint32_t>(p.stages)) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
                     }
-                    if (!ok)
-                        break;
-                    mma_commit(bar(kBarAccFull + as));
-                    ++acc_used;
+                    __syncwarp();
+                    issued = true;
+                    if (++stage == static_cast<uint32_t>(p.stages)) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
                 if (!ok)
                     break;
-                mma_commit(bar(kBarXEmpty + xb));
-                ++x_used;
-            }
-            if (issued) {
-                // All MMAs (and the arrivals they signal) finish before teardown.
-                mma_commit(bar(kBarDrain));
-                wait1(bar(kBarDrain), 0u, abort_flag, p.timeout_ns, false);
-            }
-        }
-        __syncwarp();
-    } else {
-        // Consumer warps: warp w reads TMEM lanes 32*(w%4) .. +31 of sub-tile w/4.
-        const int t = warp >> 2;
-        const int q = warp & 3;
-        uint32_t acc_used = 0;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-            const Unit w = decode_unit<SUB>(p, u);
-            float best = __int_as_float(0x7f800000);   // +inf
-            int bi = kNone;
-            bool ok = true;
-            for (int tile = w.t_begin; tile < w.t_end; ++tile) {
-                const uint32_t as = acc_used & 1u;
-                const uint32_t aph = (acc_used >> 1) & 1u;
-                if (!(ok = wait_warp(bar(kBarAccFull + as), aph, abort_flag, p.timeout_ns, lane)))
-                    break;
-                tc_fence_after();
-                const uint32_t taddr =
-                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * kAccCols + t * NT;
-#pragma unroll
-                for (int g = 0; g < NT / 128; ++g) {
-                    __syncwarp();   // tcgen05.ld is .sync.aligned: the warp must be converged
-                    float v0[32], v1[32], v2[32], v3[32];
-                    tmem_ld_32x32b_x32(taddr + g * 128 + 0, v0);
-                    tmem_ld_32x32b_x32(taddr + g * 128 + 32, v1);
-                    tmem_ld_32x32b_x32(taddr + g * 128 + 64, v2);
-                    tmem_ld_32x32b_x32(taddr + g * 128 + 96, v3);
-                    tmem_wait_ld();
-                    if (g == NT / 128 - 1) {
-                        // Scores are in registers: hand the stage back to the MMA warp.
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(bar(kBarAccEmpty + as));
-                    }
-                    const int j0 = tile * NT + g * 128;
-                    reduce_chunk(v0, p, j0 + 0, best, bi);
-                    reduce_chunk(v1, p, j0 + 32, best, bi);
-                    reduce_chunk(v2, p, j0 + 64, best, bi);
-                    reduce_chunk(v3, p, j0 + 96, best, bi);
-                }
+                if (elect_one())
+                    mma_commit(bar(kBarAccFull + as));
+                __syncwarp();
                 ++acc_used;
             }
             if (!ok)
                 break;
-            const int row = w.row0 + t * kTileM + q * 32 + lane;
-            if (t < w.nsub && row < p.N) {
+            if (elect_one())
+                mma_commit(bar(kBarXEmpty + xb));
+            __syncwarp();
+            ++x_used;
+        }
+        if (issued) {
+            // All MMAs (and the arrivals they signal) finish before teardown.
+            if (elect_one())
+                mma_commit(bar(kBarDrain));
+            __syncwarp();
+            wait_warp(bar(kBarDrain), 0u, abort_flag, p.timeout_ns, false);
+        }
+    } else {
+        // Consumer warp w reads TMEM lanes 32*(w%4) .. +31 of sub-tile
+        // (w/4)%SUB, columns [col0, col0 + kCW) of every tile.
+        const int q = warp & 3;
+        const int t = (warp >> 2) % SUB;
+        const int h = warp / (4 * SUB);
+        const int col0 = h * kCW;
+        const uint32_t cn_col = cn_base + 4u * static_cast<uint32_t>(col0);
+        float *const cn_smem = reinterpret_cast<float *>(sbase + (cn_base - base));
+        const float kNaN = __int_as_float(0x7fc00000);
+
+        auto fetch_norms = [&](int j, float (&r)[kNormPerThread]) {
+#pragma unroll
+            for (int e = 0; e < kNormPerThread; ++e) {
+                const int i = threadIdx.x + e * kConsumerThreads;
+                r[e] = (i < NT && j + i < p.K) ? __ldg(p.cnorm + j + i) : kNaN;
+            }
+        };
+        auto publish_norms = [&](int buf, const float (&r)[kNormPerThread]) {
+#pragma unroll
+            for (int e = 0; e < kNormPerThread; ++e) {
+                const int i = threadIdx.x + e * kConsumerThreads;
+                if (i < NT)
+                    cn_smem[buf * NT + i] = r[e];
+            }
+        };
+
+        uint32_t acc_used = 0;
+        bool ok = true;
+        if (blockIdx.x < p.num_units) {
+            float r[kNormPerThread];
+            fetch_norms(decode_unit<SUB>(p, blockIdx.x).t_begin * NT, r);
+            publish_norms(0, r);
+        }
+        named_bar_sync(kConsumerBarrier, kConsumerThreads);
+
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            const Unit w = decode_unit<SUB>(p, u);
+            float best = __int_as_float(0x7f800000);   // +inf
+            int bi = kNone;
+            for (int tile = w.t_begin; tile < w.t_end; ++tile, ++acc_used) {
+                // Norms of the tile after this one (possibly in the next unit).
+                int jn = -1;
+                if (tile + 1 < w.t_end)
+                    jn = (tile + 1) * NT;
+                else if (u + static_cast<int>(gridDim.x) < p.num_units)
+                    jn = decode_unit<SUB>(p, u + gridDim.x).t_begin * NT;
+                float pre[kNormPerThread];
+                if (jn >= 0)
+                    fetch_norms(jn, pre);
+
+                const uint32_t as = acc_used & 1u;
+                const uint32_t aph = (acc_used >> 1) & 1u;
+                if (ok)
+                    ok = wait_warp(bar(kBarAccFull + as), aph, abort_flag, p.timeout_ns);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                           as * kAccCols + t * NT + col0;
+                    const uint32_t cn_tile = cn_col + 4u * NT * as;
+#pragma unroll
+                    for (int g = 0; g < kGroups; ++g) {
+                        __syncwarp();   // tcgen05.ld is .sync.aligned
+                        float v[kGroup][32];
+#pragma unroll
+                        for (int c = 0; c < kGroup; ++c)
+                            tmem_ld_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c]);
+                        tmem_wait_ld();
+                        if (g == kGroups - 1) {
+                            // Scores are in registers: hand the stage back.
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(bar(kBarAccEmpty + as));
+                        }
+                        float m[kGroup];
+#pragma unroll
+                        for (int c = 0; c < kGroup; ++c) {
+                            apply_norms(v[c], cn_tile + 128u * (g * kGroup + c));
+                            m[c] = chunk_min(v[c]);
+                        }
+                        const int jg = tile * NT + col0 + g * kGroup * 32;
+#pragma unroll
+                        for (int c = 0; c < kGroup; ++c)
+                            fold_chunk(v[c], m[c], jg + 32 * c, best, bi);
+                    }
+                }
+                if (jn >= 0)
+                    publish_norms(static_cast<int>(as ^ 1u), pre);
+                named_bar_sync(kConsumerBarrier, kConsumerThreads);
+            }
+
+            // Merge the column slices of each point: (score, index) order.
+            const int lrow = t * kTileM + q * 32 + lane;
+            if (CH > 1) {
+                float *red_s = reinterpret_cast<float *>(sbase + (red_base - base));
+                int *red_i = reinterpret_cast<int *>(red_s + (CH - 1) * SUB * kTileM);
+                if (h > 0) {
+                    red_s[(h - 1) * SUB * kTileM + lrow] = best;
+                    red_i[(h - 1) * SUB * kTileM + lrow] = bi;
+                }
+                named_bar_sync(kConsumerBarrier, kConsumerThreads);
+                if (h == 0) {
+#pragma unroll
+                    for (int o = 0; o < CH - 1; ++o) {
+                        const float b2 = red_s[o * SUB * kTileM + lrow];
+                        const int i2 = red_i[o * SUB * kTileM + lrow];
+                        if (b2 < best || (b2 == best && i2 < bi)) {
+                            best = b2;
+                            bi = i2;
+                        }
+                    }
+                }
+            }
+            const int row = w.row0 + lrow;
+            if (ok && h == 0 && t < w.nsub && row < p.N) {
                 if (p.keys == nullptr) {
                     float ms;
                     int ix;
                     if (bi == kNone) {
                         ix = 0;
-                        ms = __int_as_float(0x7fc00000);
+                        ms = kNaN;
                     } else {
                         ix = bi;
                         ms = (__float_as_uint(best) == 0x80000000u) ? 0.0f : best;
@@ -427,50 +530,77 @@ __global__ void __launch_bounds__(32 * (4 * SUB + 2), 1)
     }
 }
 
-template <int SUB, int NT>
+template <int SUB, int NT, int CH, int KB>
 cudaError_t prepare_one(size_t smem)
 {
-    return cudaFuncSetAttribute(assign_kernel<SUB, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem));
+    return cudaFuncSetAttribute(assign_kernel<SUB, NT, CH, KB>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
 }
 
-template <int SUB, int NT>
+template <int SUB, int NT, int CH, int KB>
 cudaError_t launch_one(const AssignParams &p, const CUtensorMap &xmap, const CUtensorMap &cmap,
                        int grid, size_t smem, cudaStream_t stream)
 {
-    assign_kernel<SUB, NT><<<grid, 32 * (4 * SUB + 2), smem, stream>>>(xmap, cmap, p);
+    assign_kernel<SUB, NT, CH, KB><<<grid, 32 * (4 * SUB * CH + 2), smem, stream>>>(xmap, cmap, p);
     return cudaGetLastError();
+}
+
+template <int SUB, int NT, int CH>
+cudaError_t dispatch_kb(bool prepare, int kb, const AssignParams *p, const CUtensorMap *xmap,
+                        const CUtensorMap *cmap, int grid, size_t smem, cudaStream_t stream)
+{
+    switch (kb) {
+    case 1:
+        return prepare ? prepare_one<SUB, NT, CH, 1>(smem)
+                       : launch_one<SUB, NT, CH, 1>(*p, *xmap, *cmap, grid, smem, stream);
+    case 2:
+        return prepare ? prepare_one<SUB, NT, CH, 2>(smem)
+                       : launch_one<SUB, NT, CH, 2>(*p, *xmap, *cmap, grid, smem, stream);
+    case 3:
+        return prepare ? prepare_one<SUB, NT, CH, 3>(smem)
+                       : launch_one<SUB, NT, CH, 3>(*p, *xmap, *cmap, grid, smem, stream);
+    case 4:
+        return prepare ? prepare_one<SUB, NT, CH, 4>(smem)
+                       : launch_one<SUB, NT, CH, 4>(*p, *xmap, *cmap, grid, smem, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t dispatch(bool prepare, const Variant &v, int kb, const AssignParams *p,
+                     const CUtensorMap *xmap, const CUtensorMap *cmap, int grid, size_t smem,
+                     cudaStream_t stream)
+{
+    if (v.sub == 1 && v.nt == 128 && v.ch == 1)
+        return dispatch_kb<1, 128, 1>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+    if (v.sub == 1 && v.nt == 256 && v.ch == 2)
+        return dispatch_kb<1, 256, 2>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+    if (v.sub == 2 && v.nt == 128 && v.ch == 1)
+        return dispatch_kb<2, 128, 1>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-size_t assign_smem_bytes(int sub, int nt, int kblocks, int stages, int xbufs)
+const Variant kVariants[kNumVariants] = {{2, 128, 1}, {1, 256, 2}, {1, 128, 1}};
+
+size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 {
-    return 1024 + static_cast<size_t>(xbufs) * sub * kblocks * kXTileBytes +
-           static_cast<size_t>(stages) * nt * 128 + kMiscBytes;
+    return 1024 + static_cast<size_t>(xbufs) * v.sub * kblocks * kXTileBytes +
+           static_cast<size_t>(stages) * v.nt * 128 + 2 * v.nt * 4 +
+           static_cast<size_t>(v.ch - 1) * v.sub * kTileM * 8 + kMiscBytes;
 }
 
-cudaError_t assign_prepare(int sub, int nt, size_t smem)
+cudaError_t assign_prepare(const Variant &v, int kblocks, size_t smem)
 {
-    if (sub == 1 && nt == 128)
-        return prepare_one<1, 128>(smem);
-    if (sub == 1 && nt == 256)
-        return prepare_one<1, 256>(smem);
-    if (sub == 2 && nt == 128)
-        return prepare_one<2, 128>(smem);
-    return cudaErrorInvalidValue;
+    return dispatch(true, v, kblocks, nullptr, nullptr, nullptr, 0, smem, nullptr);
 }
 
-cudaError_t launch_assign(int sub, int nt, const AssignParams &p, const CUtensorMap &xmap,
-                          const CUtensorMap &cmap, int grid, size_t smem, cudaStream_t stream)
+cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
+                          const CUtensorMap &xmap, const CUtensorMap &cmap, int grid, size_t smem,
+                          cudaStream_t stream)
 {
-    if (sub == 1 && nt == 128)
-        return launch_one<1, 128>(p, xmap, cmap, grid, smem, stream);
-    if (sub == 1 && nt == 256)
-        return launch_one<1, 256>(p, xmap, cmap, grid, smem, stream);
-    if (sub == 2 && nt == 128)
-        return launch_one<2, 128>(p, xmap, cmap, grid, smem, stream);
-    return cudaErrorInvalidValue;
+    return dispatch(false, v, kblocks, &p, &xmap, &cmap, grid, smem, stream);
 }
 
 cudaError_t status_read_and_clear(int *code)

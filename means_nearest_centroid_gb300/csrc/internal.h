@@ -34,11 +34,20 @@ struct AssignParams {
     uint64_t timeout_ns;           // bound on every pipeline wait
 };
 
-size_t assign_smem_bytes(int sub, int nt, int kblocks, int stages, int xbufs);
-cudaError_t assign_prepare(int sub, int nt, size_t smem_bytes);
-cudaError_t launch_assign(int sub, int nt, const AssignParams &p, const CUtensorMap &xmap,
-                          const CUtensorMap &cmap, int grid, size_t smem_bytes,
-                          cudaStream_t stream);
+// Compiled shapes of the assignment kernel: `sub` 128-point sub-tiles per
+// block, `nt` centroids per tensor-core tile, each tile's columns split over
+// `ch` groups of consumer warps.
+struct Variant {
+    int sub, nt, ch;
+};
+constexpr int kNumVariants = 3;
+extern const Variant kVariants[kNumVariants];
+
+size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs);
+cudaError_t assign_prepare(const Variant &v, int kblocks, size_t smem_bytes);
+cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
+                          const CUtensorMap &xmap, const CUtensorMap &cmap, int grid,
+                          size_t smem_bytes, cudaStream_t stream);
 
 cudaError_t launch_norms(const void *C, int64_t K, int64_t D, float *cnorm, cudaStream_t stream);
 cudaError_t launch_finalize(const unsigned long long *keys, int64_t N, int32_t *idx,
