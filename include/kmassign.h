@@ -59,7 +59,8 @@ enum kmassign_status {
     KMASSIGN_ERR_CUDA = -5,          /* a CUDA runtime/driver call failed */
     KMASSIGN_ERR_TIMEOUT = -6,       /* a bounded wait inside a kernel ran out */
     KMASSIGN_ERR_NOT_DEVICE = -7,    /* a pointer is not device memory */
-    KMASSIGN_ERR_ARG = -8            /* an invalid plan value in kmassign_ex */
+    KMASSIGN_ERR_ARG = -8,           /* an invalid plan value in kmassign_ex */
+    KMASSIGN_ERR_SCRATCH = -9        /* too large for kmassign_noalloc's static scratch */
 };
 
 /*
@@ -119,6 +120,32 @@ int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out6);
  * check, KMASSIGN_ERR_CUDA if the stream reports an error, else KMASSIGN_OK.
  */
 int kmassign_check(void *stream);
+
+/*
+ * kmassign without any device allocation.  The pages have no counterpart to
+ * this call; it exists for callers that cannot let a library allocate device
+ * memory while they run -- a host framework that hands a plugin only its
+ * buffers and a stream and owns all device memory, or a service that fixes
+ * its memory budget at start-up because cudaMalloc/cudaFree can synchronise
+ * the device.
+ *
+ * Same arguments, layout, results and errors as kmassign.  Its temporaries
+ * live in one static device array of this library (6 MiB, held on every GPU
+ * that loads the library until the process exits) instead of the stream
+ * allocator; it calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - cnorm == NULL needs K <= 1,048,576 (the norms go into the array);
+ *     larger K returns KMASSIGN_ERR_SCRATCH before anything is launched.
+ *   - A split centroid range keeps one 8-byte key per point in the array;
+ *     for N > 262,144 the call plans without a split instead.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array and overwrites
+ * what the previous call left there, so calls whose work overlaps on the GPU
+ * (different streams, or different host threads) race; order them on one
+ * stream or synchronise between them.
+ */
+int kmassign_noalloc(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                     int64_t D, int32_t *idx, float *minscore, void *stream);
 
 /* Static English text for a status code (never NULL). */
 const char *kmassign_strerror(int code);

@@ -23,6 +23,7 @@ from . import _build
 
 __all__ = [
     "KmassignError", "library", "library_path", "kmassign", "kmassign_ex", "kmassign_norms",
+    "kmassign_noalloc",
     "kmassign_plan", "kmassign_check", "kmassign_strerror", "assign", "norms", "assign_host",
     "STATUS",
 ]
@@ -37,6 +38,7 @@ STATUS = {
     "KMASSIGN_ERR_TIMEOUT": -6,
     "KMASSIGN_ERR_NOT_DEVICE": -7,
     "KMASSIGN_ERR_ARG": -8,
+    "KMASSIGN_ERR_SCRATCH": -9,
 }
 _NAMES = {v: k for k, v in STATUS.items()}
 
@@ -62,6 +64,8 @@ def _declare(lib):
     lib.kmassign.restype = i32
     lib.kmassign_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, vp]
     lib.kmassign_ex.restype = i32
+    lib.kmassign_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp]
+    lib.kmassign_noalloc.restype = i32
     lib.kmassign_plan.argtypes = [i64, i64, i64, vp]
     lib.kmassign_plan.restype = i32
     lib.kmassign_check.argtypes = [vp]
@@ -170,6 +174,33 @@ def kmassign(X, C, cnorm=None, idx=None, minscore=None, stream=None):
     rc = library().kmassign(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, _ptr(idx), _ptr(minscore),
                             _stream_ptr(stream))
     _check(rc, "kmassign")
+    return idx
+
+
+def kmassign_noalloc(X, C, cnorm=None, idx=None, minscore=None, stream=None):
+    """kmassign for callers that cannot let the library allocate device memory.
+
+    The library's temporaries come from its static device array instead of
+    the stream allocator (see ``include/kmassign.h``).  ``idx`` should be
+    passed preallocated by such callers; it is allocated here only for
+    convenience.  Calls that overlap on the GPU share that array and race.
+    """
+    _need_cuda(X, "X", torch.bfloat16)
+    _need_cuda(C, "C", torch.bfloat16)
+    N, D = X.shape
+    K, D2 = C.shape
+    if D != D2:
+        raise ValueError("X and C disagree on D")
+    if cnorm is not None:
+        _need_cuda(cnorm, "cnorm", torch.float32)
+    if idx is None:
+        idx = torch.empty(N, dtype=torch.int32, device=X.device)
+    _need_cuda(idx, "idx", torch.int32)
+    if minscore is not None:
+        _need_cuda(minscore, "minscore", torch.float32)
+    rc = library().kmassign_noalloc(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, _ptr(idx),
+                                    _ptr(minscore), _stream_ptr(stream))
+    _check(rc, "kmassign_noalloc")
     return idx
 
 

@@ -299,7 +299,137 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// kmassign_noalloc: the assignment call for callers that must not allocate.
+//
+// Some callers cannot have a library allocate device memory behind their
+// back: a host framework that hands a plugin only its buffers and a stream
+// and owns every byte of device memory, or a service that fixes its memory
+// budget at start-up because cudaMalloc/cudaFree can synchronise the device
+// and stall other work.  For them, the two temporaries of kmassign (the norm
+// buffer when cnorm is NULL, and the packed keys of a split centroid range)
+// live in the file-scope array below instead of the stream-ordered allocator.
+// Every GPU that loads this library holds the array until the process exits.
+constexpr int64_t kNoAllocNormMax = int64_t(1) << 20;   // K, when cnorm is NULL
+constexpr int64_t kNoAllocKeyMax = int64_t(1) << 18;    // N, for a split centroid range
+constexpr size_t kNoAllocNormBytes = static_cast<size_t>(kNoAllocNormMax) * 4;
+constexpr size_t kNoAllocBytes = kNoAllocNormBytes + static_cast<size_t>(kNoAllocKeyMax) * 8;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+
+void *g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device.  The array's name in host code is only a host-side handle.
+int noalloc_scratch(unsigned char **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return KMASSIGN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return KMASSIGN_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = static_cast<unsigned char *>(g_noalloc_addr[dev]);
+    return KMASSIGN_OK;
+}
+
+int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                       int64_t D, int32_t *idx, float *minscore, cudaStream_t stream)
+{
+    int rc = check_shape(N, K, D);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    if (N == 0)
+        return KMASSIGN_OK;
+    if (X == nullptr || C == nullptr || idx == nullptr)
+        return KMASSIGN_ERR_NULL;
+    if (!aligned(X, 16) || !aligned(C, 16) || (cnorm && !aligned(cnorm, 16)) || !aligned(idx, 4) ||
+        (minscore && !aligned(minscore, 4)))
+        return KMASSIGN_ERR_ALIGN;
+    if (cnorm == nullptr && K > kNoAllocNormMax)
+        return KMASSIGN_ERR_SCRATCH;
+    const void *ptrs[5] = {X, C, cnorm, idx, minscore};
+    if ((rc = check_device_ptrs(ptrs, 5)) != KMASSIGN_OK)
+        return rc;
+
+    DeviceInfo dev;
+    if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
+        return rc;
+    Plan plan;
+    if ((rc = make_plan(N, K, D, dev, 0, 0, 0, &plan)) != KMASSIGN_OK)
+        return rc;
+    // Keys for more points than the array holds: plan without a split.
+    if (plan.ksplit > 1 && N > kNoAllocKeyMax &&
+        (rc = make_plan(N, K, D, dev, 1, 0, 0, &plan)) != KMASSIGN_OK)
+        return rc;
+
+    CUtensorMap xmap, cmap;
+    if (!encode_map(&xmap, X, static_cast<uint64_t>(N), static_cast<uint64_t>(D), kma::kTileM) ||
+        !encode_map(&cmap, C, static_cast<uint64_t>(K), static_cast<uint64_t>(D),
+                    static_cast<uint32_t>(plan.v.nt)))
+        return KMASSIGN_ERR_CUDA;
+
+    unsigned char *scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch)) != KMASSIGN_OK)
+        return rc;
+    float *norms = reinterpret_cast<float *>(scratch);
+    unsigned long long *keys = nullptr;
+    if (cnorm == nullptr) {
+        // Every norm the kernel reads is written here first.
+        if (kma::launch_norms(C, K, D, norms, stream) != cudaSuccess)
+            return KMASSIGN_ERR_CUDA;
+        cnorm = norms;
+    }
+    if (plan.ksplit > 1) {
+        // The array keeps the previous call's keys: reset them to "no candidate".
+        keys = reinterpret_cast<unsigned long long *>(scratch + kNoAllocNormBytes);
+        if (cudaMemsetAsync(keys, 0xff, static_cast<size_t>(N) * 8, stream) != cudaSuccess)
+            return KMASSIGN_ERR_CUDA;
+    }
+    AssignParams p{};
+    p.cnorm = cnorm;
+    p.idx = idx;
+    p.minscore = minscore;
+    p.keys = keys;
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.D = static_cast<int32_t>(D);
+    p.ksteps = static_cast<int32_t>(D / 16);
+    p.kblocks = static_cast<int32_t>(cdiv(D, kma::kKBlock));
+    p.rowtiles = plan.rowtiles;
+    p.ksplit = plan.ksplit;
+    p.chunk_tiles = plan.chunk_tiles;
+    p.ntiles = plan.ntiles;
+    p.num_units = plan.units;
+    p.stages = plan.stages;
+    p.xbufs = plan.xbufs;
+    p.timeout_ns = kDefaultTimeoutNs;
+    if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, plan.grid, plan.smem, stream) !=
+        cudaSuccess)
+        return KMASSIGN_ERR_CUDA;
+    if (keys != nullptr && kma::launch_finalize(keys, N, idx, minscore, stream) != cudaSuccess)
+        return KMASSIGN_ERR_CUDA;
+    return KMASSIGN_OK;
+}
+
+}  // namespace
+
 extern "C" {
+
+int kmassign_noalloc(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                     int64_t D, int32_t *idx, float *minscore, void *stream)
+{
+    return run_assign_noalloc(X, C, cnorm, N, K, D, idx, minscore,
+                              static_cast<cudaStream_t>(stream));
+}
 
 int kmassign_norms(const void *C, int64_t K, int64_t D, float *cnorm, void *stream)
 {
@@ -384,6 +514,8 @@ const char *kmassign_strerror(int code)
         return "a bounded pipeline wait inside a kernel ran out; the kernel drained and returned";
     case KMASSIGN_ERR_NOT_DEVICE:
         return "a pointer is not device memory of the current device";
+    case KMASSIGN_ERR_SCRATCH:
+        return "kmassign_noalloc: K exceeds its static norm buffer (cnorm NULL needs K <= 1048576)";
     case KMASSIGN_ERR_ARG:
         return "invalid plan value (ksplit >= 0, rows_per_cta 128/256, centroids_per_tile "
                "128/256, not both 256)";
