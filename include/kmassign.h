@@ -93,26 +93,34 @@ int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_
 
 /*
  * kmassign with an explicit plan (0 = the automatic choice for each field):
- *   ksplit              number of centroid ranges the K axis is split into;
- *                       > 1 merges partial winners with a 64-bit atomicMin
- *                       on (ordered score bits << 32 | index) keys
+ *   ksplit              number of centroid ranges the K axis of every row
+ *                       tile is split into; > 1 merges partial winners with a
+ *                       64-bit atomicMin on (ordered score bits << 32 | index)
+ *                       keys.  ksplit <= -2 splits only the row tiles of the
+ *                       last, partial wave of thread blocks into -ksplit
+ *                       ranges (wave-tail balancing); -1 is invalid
  *   rows_per_cta        128 or 256 points per thread block tile
  *   centroids_per_tile  128 or 256 centroids per tensor-core tile
  *                       (rows_per_cta 256 requires 128)
- * Same arguments, layout and errors as kmassign; a value outside these sets
- * returns KMASSIGN_ERR_ARG.  Tests use it to cover every path.
+ *   consumer_warps      warps reducing the score tiles: 4 (128x128 tiles),
+ *                       8 or 16 (128x256 and 256x128 tiles)
+ * Same arguments, layout and errors as kmassign; a value outside these sets,
+ * or a combination no compiled kernel has, returns KMASSIGN_ERR_ARG.  Tests
+ * use it to cover every path.
  */
 int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
                 int64_t D, int32_t *idx, float *minscore, int ksplit, int rows_per_cta,
-                int centroids_per_tile, void *stream);
+                int centroids_per_tile, int consumer_warps, void *stream);
 
 /*
  * The plan kmassign would choose for (N, K, D) on the current device:
- * out[0] = ksplit, out[1] = rows_per_cta, out[2] = centroids_per_tile,
- * out[3] = thread blocks launched, out[4] = shared-memory ring stages,
- * out[5] = X tile buffers.  Launches nothing.
+ * out[0] = ksplit of the split row tiles (1: none split), out[1] =
+ * rows_per_cta, out[2] = centroids_per_tile, out[3] = thread blocks
+ * launched, out[4] = shared-memory ring stages, out[5] = X tile buffers,
+ * out[6] = row tiles processed whole, out[7] = row tiles split, out[8] =
+ * consumer warps.  Launches nothing.
  */
-int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out6);
+int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9);
 
 /*
  * Synchronise `stream`, then report and clear the device status word:

@@ -62,7 +62,7 @@ def _declare(lib):
     lib.kmassign_norms.restype = i32
     lib.kmassign.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.kmassign.restype = i32
-    lib.kmassign_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, vp]
+    lib.kmassign_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, i32, vp]
     lib.kmassign_ex.restype = i32
     lib.kmassign_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.kmassign_noalloc.restype = i32
@@ -134,7 +134,8 @@ def kmassign_norms(C: torch.Tensor, out: torch.Tensor | None = None, stream=None
 
 
 def kmassign_ex(X, C, cnorm=None, idx=None, minscore=None, ksplit: int = 0,
-                rows_per_cta: int = 0, centroids_per_tile: int = 0, stream=None):
+                rows_per_cta: int = 0, centroids_per_tile: int = 0, consumer_warps: int = 0,
+                stream=None):
     """Assignment with an explicit plan (0 = automatic).  Returns idx (int32)."""
     _need_cuda(X, "X", torch.bfloat16)
     _need_cuda(C, "C", torch.bfloat16)
@@ -151,7 +152,7 @@ def kmassign_ex(X, C, cnorm=None, idx=None, minscore=None, ksplit: int = 0,
         _need_cuda(minscore, "minscore", torch.float32)
     rc = library().kmassign_ex(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, _ptr(idx), _ptr(minscore),
                                int(ksplit), int(rows_per_cta), int(centroids_per_tile),
-                               _stream_ptr(stream))
+                               int(consumer_warps), _stream_ptr(stream))
     _check(rc, "kmassign_ex")
     return idx
 
@@ -205,10 +206,11 @@ def kmassign_noalloc(X, C, cnorm=None, idx=None, minscore=None, stream=None):
 
 
 def kmassign_plan(N: int, K: int, D: int) -> dict:
-    out = (ctypes.c_int32 * 6)()
+    out = (ctypes.c_int32 * 9)()
     _check(library().kmassign_plan(int(N), int(K), int(D), ctypes.cast(out, ctypes.c_void_p)),
            "kmassign_plan")
-    keys = ["ksplit", "rows_per_cta", "centroids_per_tile", "grid", "stages", "xbufs"]
+    keys = ["ksplit", "rows_per_cta", "centroids_per_tile", "grid", "stages", "xbufs",
+            "whole_row_tiles", "split_row_tiles", "consumer_warps"]
     return dict(zip(keys, list(out)))
 
 

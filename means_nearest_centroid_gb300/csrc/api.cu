@@ -134,25 +134,37 @@ struct Plan {
     kma::Variant v;
     int ksplit, grid, stages, xbufs;
     int rowtiles, ntiles, chunk_tiles, units;
+    int full_units, split_row0;   // see AssignParams
     size_t smem;
 };
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Units u < X with u % P == b under the static round-robin schedule.
+int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b - 1) / P + 1 : 0; }
+
 // Pick the kernel shape and the centroid split from a cost model in SM
-// clocks per centroid tile, fitted to measurements of the kernel on GB300:
+// clocks per centroid tile, fitted to measurements of the kernel on GB300
+// (the five benchmark workloads, every shape forced in turn):
 //   * tensor pipe: a 128x256x16 bf16 MMA takes 128 clocks back to back, a
-//     128x128x16 one ~80 with two accumulators and ~92 with one, plus a
-//     per-tile hand-over cost;
-//   * epilogue: the consumer warps need ~3000 clocks per 128x256 tile with 8
-//     warps, ~2500 per 256x128 tile with 8 warps, ~2000 per 128x128 tile
-//     with 4 warps (latency-bound; measured on iid and clustered data);
-//   * a unit pays ~2500 clocks to load its X tile and fill the pipe; a split
-//     pays ~6000 clocks for the key memset and the finalize kernel.
+//     128x128x16 one ~80 with two accumulators and ~92 with one, plus ~500
+//     clocks of hand-over per tile;
+//   * epilogue floor per tile (latency-bound reduction): ~2150 clocks for a
+//     128x256 tile with 8 or 16 warps, ~1700 / ~1550 for a 256x128 tile with
+//     8 / 16 warps, ~1400 for a 128x128 tile with 4 warps;
+//   * a unit pays ~5000 clocks to load its X tile and fill the pipe;
+//   * any split pays ~12000 clocks for the key memset, the finalize kernel
+//     and their launches.
+// Splits considered: every row tile into ks centroid ranges (ks >= 1), or
+// only the row tiles of the last partial wave (the rest stay whole), which
+// evens out the last wave when there are a few waves of whole row tiles.
+// force_ksplit > 0 forces a uniform split, < -1 a tail split into
+// -force_ksplit ranges.
 int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_ksplit,
-              int force_rows, int force_nt, Plan *out)
+              int force_rows, int force_nt, int force_cw, Plan *out)
 {
     const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
+    const int64_t P = dev.sms;
     bool found = false;
     double best_cost = 0.0;
     Plan best{};
@@ -160,6 +172,8 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         if (force_rows != 0 && force_rows != v.sub * kma::kTileM)
             continue;
         if (force_nt != 0 && force_nt != v.nt)
+            continue;
+        if (force_cw != 0 && force_cw != 4 * v.sub * v.ch)
             continue;
         const size_t xbytes = static_cast<size_t>(v.sub) * kblocks * kma::kXTileBytes;
         const size_t stage_bytes = static_cast<size_t>(v.nt) * 128;
@@ -171,38 +185,67 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const int stages = static_cast<int>(std::min<size_t>(
             kma::kMaxStages, (budget - fixed - xbufs * xbytes) / stage_bytes));
         const int64_t ntiles = cdiv(K, v.nt);
-        const int64_t rowtiles = cdiv(N, static_cast<int64_t>(v.sub) * kma::kTileM);
+        const int64_t R = cdiv(N, static_cast<int64_t>(v.sub) * kma::kTileM);
         const double mma_clk = v.nt == 256 ? 128.0 : (v.sub == 2 ? 80.0 : 92.0);
-        const double tile_mma = double(v.sub) * kblocks * 4 * mma_clk + (v.nt == 256 ? 700 : 500);
-        const double tile_epi = v.nt == 256 ? 3000.0 : (v.sub == 2 ? 2480.0 : 2000.0);
+        const double tile_mma = double(v.sub) * kblocks * 4 * mma_clk + 500.0;
+        const double tile_epi = v.nt == 256 ? 2150.0
+                                : v.sub == 2 ? (v.ch == 2 ? 1550.0 : 1700.0) : 1400.0;
         const double tile = std::max(tile_mma, tile_epi);
-        int64_t ks_lo = 1, ks_hi = std::min<int64_t>(ntiles, 64);
-        if (force_ksplit > 0)
-            ks_lo = ks_hi = std::min<int64_t>(force_ksplit, ntiles);
-        for (int64_t ks = ks_lo; ks <= ks_hi; ++ks) {
+        const double unit_over = 5000.0;
+
+        // Candidate (F whole row tiles, split the rest into ks ranges).
+        auto consider = [&](int64_t F, int64_t ks) {
             const int64_t chunk = cdiv(ntiles, ks);
             const int64_t ks_eff = cdiv(ntiles, chunk);
-            if (ks_eff != ks && force_ksplit <= 0)
-                continue;
-            const int64_t units = rowtiles * ks_eff;
-            if (units >= (int64_t(1) << 31))
-                continue;
-            const int64_t waves = cdiv(units, dev.sms);
-            const double cost = double(waves) * (double(chunk) * tile + 2500.0) +
-                                (ks_eff > 1 ? 6000.0 : 0.0);
-            if (!found || cost < best_cost * 0.98) {
+            const int64_t split_rows = R - F;
+            const int64_t units = F + split_rows * ks_eff;
+            if (units >= (int64_t(1) << 31) || units <= 0)
+                return;
+            const bool any_split = split_rows > 0 && ks_eff > 1;
+            const int64_t full_units = any_split ? F : R;   // ks 1: nothing is split
+            const int64_t split_row0 = any_split ? F : R;
+            const int64_t nunits = full_units + (R - split_row0) * (any_split ? ks_eff : 1);
+            double worst = 0.0;
+            for (int64_t b = 0; b < std::min<int64_t>(P, nunits); ++b) {
+                const int64_t nf = units_of_block(full_units, P, b);
+                const int64_t ns = units_of_block(nunits, P, b) - nf;
+                const double c = double(nf) * (double(ntiles) * tile + unit_over) +
+                                 double(ns) * (double(chunk) * tile + unit_over);
+                worst = std::max(worst, c);
+            }
+            const double cost = worst + (any_split ? 12000.0 : 0.0);
+            if (!found || cost < best_cost * 0.995) {
                 found = true;
                 best_cost = cost;
                 best.v = v;
-                best.ksplit = static_cast<int>(ks_eff);
-                best.rowtiles = static_cast<int>(rowtiles);
+                best.ksplit = any_split ? static_cast<int>(ks_eff) : 1;
+                best.rowtiles = static_cast<int>(R);
                 best.ntiles = static_cast<int>(ntiles);
-                best.chunk_tiles = static_cast<int>(chunk);
-                best.units = static_cast<int>(units);
-                best.grid = static_cast<int>(std::min<int64_t>(units, dev.sms));
+                best.chunk_tiles = any_split ? static_cast<int>(chunk) : static_cast<int>(ntiles);
+                best.full_units = static_cast<int>(full_units);
+                best.split_row0 = static_cast<int>(split_row0);
+                best.units = static_cast<int>(nunits);
+                best.grid = static_cast<int>(std::min<int64_t>(nunits, P));
                 best.stages = stages;
                 best.xbufs = xbufs;
                 best.smem = kma::assign_smem_bytes(v, kblocks, stages, xbufs);
+            }
+        };
+        if (force_ksplit > 0) {
+            const int64_t ks = std::min<int64_t>(force_ksplit, ntiles);
+            consider(ks > 1 ? 0 : R, ks);
+        } else if (force_ksplit < -1) {
+            const int64_t ks = std::min<int64_t>(-force_ksplit, ntiles);
+            const int64_t F = (R > P && R % P != 0) ? (R / P) * P : 0;
+            consider(F, ks);
+        } else {
+            for (int64_t ks = 1; ks <= std::min<int64_t>(ntiles, 64); ++ks) {
+                const int64_t chunk = cdiv(ntiles, ks);
+                if (cdiv(ntiles, chunk) != ks)
+                    continue;
+                consider(ks > 1 ? 0 : R, ks);
+                if (ks > 1 && R > P && R % P != 0 && ks <= 16)
+                    consider((R / P) * P, ks);
             }
         }
     }
@@ -212,16 +255,47 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
     return KMASSIGN_OK;
 }
 
+// Fill the kernel parameters of a plan.
+AssignParams make_params(const Plan &plan, const float *cnorm, int32_t *idx, float *minscore,
+                         unsigned long long *keys, int64_t N, int64_t K, int64_t D)
+{
+    AssignParams p{};
+    p.cnorm = cnorm;
+    p.idx = idx;
+    p.minscore = minscore;
+    p.keys = keys;
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.D = static_cast<int32_t>(D);
+    p.ksteps = static_cast<int32_t>(D / 16);
+    p.kblocks = static_cast<int32_t>(cdiv(D, kma::kKBlock));
+    p.rowtiles = plan.rowtiles;
+    p.full_units = plan.full_units;
+    p.split_row0 = plan.split_row0;
+    p.ksplit = plan.ksplit;
+    p.chunk_tiles = plan.chunk_tiles;
+    p.ntiles = plan.ntiles;
+    p.num_units = plan.units;
+    p.stages = plan.stages;
+    p.xbufs = plan.xbufs;
+    p.timeout_ns = kDefaultTimeoutNs;
+    return p;
+}
+
+// First point whose answer goes through the packed keys, and their count.
+int64_t split_first_row(const Plan &plan) { return int64_t(plan.split_row0) * plan.v.sub * kma::kTileM; }
+
 int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
                int32_t *idx, float *minscore, int force_ksplit, int force_rows, int force_nt,
-               cudaStream_t stream)
+               int force_cw, cudaStream_t stream)
 {
     int rc = check_shape(N, K, D);
     if (rc != KMASSIGN_OK)
         return rc;
-    if (force_ksplit < 0 || (force_rows != 0 && force_rows != 128 && force_rows != 256) ||
+    if (force_ksplit == -1 || (force_rows != 0 && force_rows != 128 && force_rows != 256) ||
         (force_nt != 0 && force_nt != 128 && force_nt != 256) ||
-        (force_rows == 256 && force_nt == 256))
+        (force_rows == 256 && force_nt == 256) ||
+        (force_cw != 0 && force_cw != 4 && force_cw != 8 && force_cw != 16))
         return KMASSIGN_ERR_ARG;
     if (N == 0)
         return KMASSIGN_OK;
@@ -238,7 +312,8 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
     if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
     Plan plan;
-    if ((rc = make_plan(N, K, D, dev, force_ksplit, force_rows, force_nt, &plan)) != KMASSIGN_OK)
+    if ((rc = make_plan(N, K, D, dev, force_ksplit, force_rows, force_nt, force_cw, &plan)) !=
+        KMASSIGN_OK)
         return rc;
 
     CUtensorMap xmap, cmap;
@@ -258,36 +333,23 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
             rc = KMASSIGN_ERR_CUDA;
         cnorm = tmp_norm;
     }
-    if (rc == KMASSIGN_OK && plan.ksplit > 1) {
-        if (cudaMallocAsync(reinterpret_cast<void **>(&keys), static_cast<size_t>(N) * 8, stream) !=
-                cudaSuccess ||
-            cudaMemsetAsync(keys, 0xff, static_cast<size_t>(N) * 8, stream) != cudaSuccess)
+    const int64_t row_split = split_first_row(plan);
+    const int64_t n_split = plan.ksplit > 1 ? N - row_split : 0;
+    if (rc == KMASSIGN_OK && n_split > 0) {
+        if (cudaMallocAsync(reinterpret_cast<void **>(&keys), static_cast<size_t>(n_split) * 8,
+                            stream) != cudaSuccess ||
+            cudaMemsetAsync(keys, 0xff, static_cast<size_t>(n_split) * 8, stream) != cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
     }
     if (rc == KMASSIGN_OK) {
-        AssignParams p{};
-        p.cnorm = cnorm;
-        p.idx = idx;
-        p.minscore = minscore;
-        p.keys = keys;
-        p.N = static_cast<int32_t>(N);
-        p.K = static_cast<int32_t>(K);
-        p.D = static_cast<int32_t>(D);
-        p.ksteps = static_cast<int32_t>(D / 16);
-        p.kblocks = static_cast<int32_t>(cdiv(D, kma::kKBlock));
-        p.rowtiles = plan.rowtiles;
-        p.ksplit = plan.ksplit;
-        p.chunk_tiles = plan.chunk_tiles;
-        p.ntiles = plan.ntiles;
-        p.num_units = plan.units;
-        p.stages = plan.stages;
-        p.xbufs = plan.xbufs;
-        p.timeout_ns = kDefaultTimeoutNs;
+        const AssignParams p = make_params(plan, cnorm, idx, minscore, keys, N, K, D);
         if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, plan.grid, plan.smem, stream) !=
             cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
-        else if (keys != nullptr && kma::launch_finalize(keys, N, idx, minscore, stream) !=
-                                        cudaSuccess)
+        else if (keys != nullptr &&
+                 kma::launch_finalize(keys, n_split, idx + row_split,
+                                      minscore ? minscore + row_split : nullptr,
+                                      stream) != cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
     }
     if (keys != nullptr && cudaFreeAsync(keys, stream) != cudaSuccess)
@@ -364,11 +426,11 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
     if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
     Plan plan;
-    if ((rc = make_plan(N, K, D, dev, 0, 0, 0, &plan)) != KMASSIGN_OK)
+    if ((rc = make_plan(N, K, D, dev, 0, 0, 0, 0, &plan)) != KMASSIGN_OK)
         return rc;
     // Keys for more points than the array holds: plan without a split.
-    if (plan.ksplit > 1 && N > kNoAllocKeyMax &&
-        (rc = make_plan(N, K, D, dev, 1, 0, 0, &plan)) != KMASSIGN_OK)
+    if (plan.ksplit > 1 && N - split_first_row(plan) > kNoAllocKeyMax &&
+        (rc = make_plan(N, K, D, dev, 1, 0, 0, 0, &plan)) != KMASSIGN_OK)
         return rc;
 
     CUtensorMap xmap, cmap;
@@ -388,34 +450,21 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
             return KMASSIGN_ERR_CUDA;
         cnorm = norms;
     }
-    if (plan.ksplit > 1) {
+    const int64_t row_split = split_first_row(plan);
+    const int64_t n_split = plan.ksplit > 1 ? N - row_split : 0;
+    if (n_split > 0) {
         // The array keeps the previous call's keys: reset them to "no candidate".
         keys = reinterpret_cast<unsigned long long *>(scratch + kNoAllocNormBytes);
-        if (cudaMemsetAsync(keys, 0xff, static_cast<size_t>(N) * 8, stream) != cudaSuccess)
+        if (cudaMemsetAsync(keys, 0xff, static_cast<size_t>(n_split) * 8, stream) != cudaSuccess)
             return KMASSIGN_ERR_CUDA;
     }
-    AssignParams p{};
-    p.cnorm = cnorm;
-    p.idx = idx;
-    p.minscore = minscore;
-    p.keys = keys;
-    p.N = static_cast<int32_t>(N);
-    p.K = static_cast<int32_t>(K);
-    p.D = static_cast<int32_t>(D);
-    p.ksteps = static_cast<int32_t>(D / 16);
-    p.kblocks = static_cast<int32_t>(cdiv(D, kma::kKBlock));
-    p.rowtiles = plan.rowtiles;
-    p.ksplit = plan.ksplit;
-    p.chunk_tiles = plan.chunk_tiles;
-    p.ntiles = plan.ntiles;
-    p.num_units = plan.units;
-    p.stages = plan.stages;
-    p.xbufs = plan.xbufs;
-    p.timeout_ns = kDefaultTimeoutNs;
+    const AssignParams p = make_params(plan, cnorm, idx, minscore, keys, N, K, D);
     if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, plan.grid, plan.smem, stream) !=
         cudaSuccess)
         return KMASSIGN_ERR_CUDA;
-    if (keys != nullptr && kma::launch_finalize(keys, N, idx, minscore, stream) != cudaSuccess)
+    if (keys != nullptr &&
+        kma::launch_finalize(keys, n_split, idx + row_split,
+                             minscore ? minscore + row_split : nullptr, stream) != cudaSuccess)
         return KMASSIGN_ERR_CUDA;
     return KMASSIGN_OK;
 }
@@ -451,21 +500,21 @@ int kmassign_norms(const void *C, int64_t K, int64_t D, float *cnorm, void *stre
 int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
              int32_t *idx, float *minscore, void *stream)
 {
-    return run_assign(X, C, cnorm, N, K, D, idx, minscore, 0, 0, 0,
+    return run_assign(X, C, cnorm, N, K, D, idx, minscore, 0, 0, 0, 0,
                       static_cast<cudaStream_t>(stream));
 }
 
 int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
                 int32_t *idx, float *minscore, int ksplit, int rows_per_cta,
-                int centroids_per_tile, void *stream)
+                int centroids_per_tile, int consumer_warps, void *stream)
 {
     return run_assign(X, C, cnorm, N, K, D, idx, minscore, ksplit, rows_per_cta,
-                      centroids_per_tile, static_cast<cudaStream_t>(stream));
+                      centroids_per_tile, consumer_warps, static_cast<cudaStream_t>(stream));
 }
 
-int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out6)
+int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9)
 {
-    if (out6 == nullptr)
+    if (out9 == nullptr)
         return KMASSIGN_ERR_NULL;
     int rc = check_shape(N, K, D);
     if (rc != KMASSIGN_OK)
@@ -474,14 +523,17 @@ int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out6)
     if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
     Plan plan;
-    if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, 0, 0, 0, &plan)) != KMASSIGN_OK)
+    if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, 0, 0, 0, 0, &plan)) != KMASSIGN_OK)
         return rc;
-    out6[0] = plan.ksplit;
-    out6[1] = plan.v.sub * kma::kTileM;
-    out6[2] = plan.v.nt;
-    out6[3] = plan.grid;
-    out6[4] = plan.stages;
-    out6[5] = plan.xbufs;
+    out9[0] = plan.ksplit;
+    out9[1] = plan.v.sub * kma::kTileM;
+    out9[2] = plan.v.nt;
+    out9[3] = plan.grid;
+    out9[4] = plan.stages;
+    out9[5] = plan.xbufs;
+    out9[6] = plan.full_units;
+    out9[7] = plan.rowtiles - plan.split_row0;
+    out9[8] = 4 * plan.v.sub * plan.v.ch;
     return KMASSIGN_OK;
 }
 
@@ -517,8 +569,8 @@ const char *kmassign_strerror(int code)
     case KMASSIGN_ERR_SCRATCH:
         return "kmassign_noalloc: K exceeds its static norm buffer (cnorm NULL needs K <= 1048576)";
     case KMASSIGN_ERR_ARG:
-        return "invalid plan value (ksplit >= 0, rows_per_cta 128/256, centroids_per_tile "
-               "128/256, not both 256)";
+        return "invalid plan value (ksplit != -1, rows_per_cta 128/256, centroids_per_tile "
+               "128/256, not both 256, consumer_warps 4/8/16 matching the shape)";
     default:
         return "unknown kmassign status code";
     }

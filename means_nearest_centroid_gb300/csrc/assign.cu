@@ -23,11 +23,12 @@
 //                      fenced-load pattern of the Key ideas table), then apply
 //                      the norms and reduce.
 //
-// Centroid norms reach the consumers through shared memory: the consumer
-// threads fetch the next tile's norms from global memory while the current
-// tile is reduced and publish them behind a named barrier, so the reduction
-// reads them with broadcast shared loads (the L1 cache is mostly carved out
-// for the operand ring and would miss).
+// Centroid norms reach the consumers through shared memory: a norm warp runs
+// up to kCnStages tiles ahead, copying each tile's norms (NaN past K) into a
+// small ring guarded by full/empty mbarriers, so the reduction reads them
+// with broadcast shared loads (the L1 cache is mostly carved out for the
+// operand ring and would miss) and the consumer warps never wait on one
+// another within a unit.
 //
 // The reduction works on 32-column chunks: s = fmaf(-2, acc, cnorm) for the
 // chunk (two lanes per packed fma), the chunk minimum by a 3-input min tree
@@ -37,15 +38,18 @@
 // warp keeps the lowest index on ties; column slices and split centroid
 // ranges merge by (score, index).  A NaN score never wins.
 //
-// A work unit is (row tile, centroid range).  When the centroid axis is
-// split, partial winners meet in a 64-bit atomicMin on keys holding the
-// order-preserving score bits above the centroid index, which keeps the
-// result deterministic and the lowest index on ties.
+// A work unit is (row tile, centroid range).  When the centroid axis of a
+// row tile is split (for every row tile when there are too few of them to
+// fill the GPU, or only for the last, partial wave of row tiles -- the
+// wave-tail balancing of the GEMM page, applied along K), partial winners
+// meet in a 64-bit atomicMin on keys holding the order-preserving score bits
+// above the centroid index, which keeps the result deterministic and the
+// lowest index on ties.
 //
 // Every mbarrier wait is bounded by p.timeout_ns of %globaltimer.  A wait that
 // runs out records KMASSIGN_ERR_TIMEOUT in the status word and raises a
 // block-wide abort flag; after that every wait returns at once, consumer
-// warps skip their work but keep meeting their named barriers, the producer
+// warps skip their work but keep meeting their named barrier, the producer
 // waits (again bounded) for its copies in flight, the MMA warp waits for its
 // MMAs, and the tensor memory is freed before the block returns.
 #include "internal.h"
@@ -67,7 +71,10 @@ constexpr int kBarAccEmpty = kBarAccFull + 2;         // [2]
 constexpr int kBarDrain = kBarAccEmpty + 2;           // [1]
 constexpr int kBarCFull = kBarDrain + 1;              // [kMaxStages]
 constexpr int kBarCEmpty = kBarCFull + kMaxStages;    // [kMaxStages]
-constexpr int kNumBars = kBarCEmpty + kMaxStages;
+constexpr int kCnStages = 4;                          // centroid-norm ring depth
+constexpr int kBarCnFull = kBarCEmpty + kMaxStages;   // [kCnStages]
+constexpr int kBarCnEmpty = kBarCnFull + kCnStages;   // [kCnStages]
+constexpr int kNumBars = kBarCnEmpty + kCnStages;
 constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot + abort flag
 constexpr uint32_t kConsumerBarrier = 1;              // named barrier id
 
@@ -134,19 +141,35 @@ struct Unit {
     int32_t nsub;      // 128-point sub-tiles holding at least one point
     int32_t t_begin;   // first centroid tile
     int32_t t_end;     // one past the last centroid tile
+    bool split;        // part of a split centroid range: merge through the keys
 };
 
+// Units [0, full_units) cover one row tile and every centroid tile; the
+// remaining units split the row tiles from split_row0 on into ksplit
+// centroid ranges (all of them when full_units == 0, only the last, partial
+// wave of row tiles when the plan balances the wave tail).
 template <int SUB>
 __device__ __forceinline__ Unit decode_unit(const AssignParams &p, int u)
 {
     Unit w;
-    const int rt = u / p.ksplit;
-    const int kc = u - rt * p.ksplit;
+    int rt;
+    if (u < p.full_units) {
+        rt = u;
+        w.t_begin = 0;
+        w.t_end = p.ntiles;
+        w.split = false;
+    } else {
+        const int v = u - p.full_units;
+        const int r = v / p.ksplit;
+        const int kc = v - r * p.ksplit;
+        rt = p.split_row0 + r;
+        w.t_begin = kc * p.chunk_tiles;
+        w.t_end = min(p.ntiles, w.t_begin + p.chunk_tiles);
+        w.split = true;
+    }
     w.row0 = rt * SUB * kTileM;
     const int left = p.N - w.row0;
     w.nsub = min(SUB, (left + kTileM - 1) / kTileM);
-    w.t_begin = kc * p.chunk_tiles;
-    w.t_end = min(p.ntiles, w.t_begin + p.chunk_tiles);
     return w;
 }
 
@@ -201,7 +224,7 @@ __device__ __forceinline__ void fold_chunk(const float (&s)[32], float m, int j0
 }
 
 template <int SUB, int NT, int CH, int KB>
-__global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
+__global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
     assign_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap cmap,
                   const AssignParams p)
 {
@@ -209,6 +232,7 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
     constexpr int kConsumerThreads = 32 * kConsumerWarps;
     constexpr int kProducerWarp = kConsumerWarps;
     constexpr int kMmaWarp = kConsumerWarps + 1;
+    constexpr int kNormWarp = kConsumerWarps + 2;
     constexpr int kCW = NT / CH;                       // columns per consumer warp per tile
     constexpr int kChunks = kCW / 32;
     constexpr int kGroup = kChunks < 4 ? kChunks : 4;  // chunks loaded per tcgen05.wait::ld
@@ -218,7 +242,6 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
     constexpr uint32_t kAccCols = SUB * NT;            // columns of one accumulator stage
     constexpr uint32_t kTmemCols = 2 * kAccCols;       // two stages: 256 or 512
     constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, NT);
-    constexpr int kNormPerThread = (NT + kConsumerThreads - 1) / kConsumerThreads;
     static_assert(kTmemCols <= 512, "accumulators exceed tensor memory");
     static_assert(kCW % 32 == 0 && kChunks % kGroup == 0, "column slice must be whole chunks");
 
@@ -227,8 +250,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t x_base = base;
     const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
-    const uint32_t cn_base = c_base + p.stages * kCStageBytes;       // float[2][NT]
-    const uint32_t red_base = cn_base + 2 * NT * 4;                   // {float,int}[CH-1][SUB*128]
+    const uint32_t cn_base = c_base + p.stages * kCStageBytes;       // float[kCnStages][NT]
+    const uint32_t red_base = cn_base + kCnStages * NT * 4;           // {float,int}[CH-1][SUB*128]
     const uint32_t bar_base = red_base + (CH - 1) * SUB * kTileM * 8;
     uint8_t *const sbase = smem_raw + (base - raw);
     uint8_t *misc_ptr = smem_raw + (bar_base - raw) + kNumBars * 8;
@@ -252,6 +275,10 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
         for (int s = 0; s < kMaxStages; ++s) {
             mbar_init(bar(kBarCFull + s), 1);
             mbar_init(bar(kBarCEmpty + s), 1);
+        }
+        for (int s = 0; s < kCnStages; ++s) {
+            mbar_init(bar(kBarCnFull + s), 32);
+            mbar_init(bar(kBarCnEmpty + s), kConsumerWarps);
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -386,6 +413,28 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
             __syncwarp();
             wait_warp(bar(kBarDrain), 0u, abort_flag, p.timeout_ns, false);
         }
+    } else if (warp == kNormWarp) {
+        // Norm warp: one ring slot per tile of this block's schedule.
+        float *const cn_smem = reinterpret_cast<float *>(sbase + (cn_base - base));
+        const float kNaN = __int_as_float(0x7fc00000);
+        uint32_t n = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const Unit w = decode_unit<SUB>(p, u);
+            for (int tile = w.t_begin; tile < w.t_end; ++tile, ++n) {
+                const uint32_t b = n % kCnStages;
+                const uint32_t ph = (n / kCnStages) & 1u;
+                if (!(ok = wait_warp(bar(kBarCnEmpty + b), ph ^ 1u, abort_flag, p.timeout_ns)))
+                    break;
+                const int j = tile * NT;
+#pragma unroll
+                for (int e = 0; e < NT / 32; ++e) {
+                    const int i = e * 32 + lane;
+                    cn_smem[b * NT + i] = (j + i < p.K) ? __ldg(p.cnorm + j + i) : kNaN;
+                }
+                mbar_arrive(bar(kBarCnFull + b));   // release: this lane's stores
+            }
+        }
     } else {
         // Consumer warp w reads TMEM lanes 32*(w%4) .. +31 of sub-tile
         // (w/4)%SUB, columns [col0, col0 + kCW) of every tile.
@@ -394,58 +443,28 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
         const int h = warp / (4 * SUB);
         const int col0 = h * kCW;
         const uint32_t cn_col = cn_base + 4u * static_cast<uint32_t>(col0);
-        float *const cn_smem = reinterpret_cast<float *>(sbase + (cn_base - base));
         const float kNaN = __int_as_float(0x7fc00000);
-
-        auto fetch_norms = [&](int j, float (&r)[kNormPerThread]) {
-#pragma unroll
-            for (int e = 0; e < kNormPerThread; ++e) {
-                const int i = threadIdx.x + e * kConsumerThreads;
-                r[e] = (i < NT && j + i < p.K) ? __ldg(p.cnorm + j + i) : kNaN;
-            }
-        };
-        auto publish_norms = [&](int buf, const float (&r)[kNormPerThread]) {
-#pragma unroll
-            for (int e = 0; e < kNormPerThread; ++e) {
-                const int i = threadIdx.x + e * kConsumerThreads;
-                if (i < NT)
-                    cn_smem[buf * NT + i] = r[e];
-            }
-        };
-
         uint32_t acc_used = 0;
         bool ok = true;
-        if (blockIdx.x < p.num_units) {
-            float r[kNormPerThread];
-            fetch_norms(decode_unit<SUB>(p, blockIdx.x).t_begin * NT, r);
-            publish_norms(0, r);
-        }
-        named_bar_sync(kConsumerBarrier, kConsumerThreads);
 
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             const Unit w = decode_unit<SUB>(p, u);
             float best = __int_as_float(0x7f800000);   // +inf
             int bi = kNone;
             for (int tile = w.t_begin; tile < w.t_end; ++tile, ++acc_used) {
-                // Norms of the tile after this one (possibly in the next unit).
-                int jn = -1;
-                if (tile + 1 < w.t_end)
-                    jn = (tile + 1) * NT;
-                else if (u + static_cast<int>(gridDim.x) < p.num_units)
-                    jn = decode_unit<SUB>(p, u + gridDim.x).t_begin * NT;
-                float pre[kNormPerThread];
-                if (jn >= 0)
-                    fetch_norms(jn, pre);
-
                 const uint32_t as = acc_used & 1u;
                 const uint32_t aph = (acc_used >> 1) & 1u;
+                const uint32_t nb = acc_used % kCnStages;
+                const uint32_t nph = (acc_used / kCnStages) & 1u;
                 if (ok)
                     ok = wait_warp(bar(kBarAccFull + as), aph, abort_flag, p.timeout_ns);
+                if (ok)
+                    ok = wait_warp(bar(kBarCnFull + nb), nph, abort_flag, p.timeout_ns);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                            as * kAccCols + t * NT + col0;
-                    const uint32_t cn_tile = cn_col + 4u * NT * as;
+                    const uint32_t cn_tile = cn_col + 4u * NT * nb;
 #pragma unroll
                     for (int g = 0; g < kGroups; ++g) {
                         __syncwarp();   // tcgen05.ld is .sync.aligned
@@ -472,10 +491,11 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
                         for (int c = 0; c < kGroup; ++c)
                             fold_chunk(v[c], m[c], jg + 32 * c, best, bi);
                     }
+                    // This warp is done with the tile's norms.
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(bar(kBarCnEmpty + nb));
                 }
-                if (jn >= 0)
-                    publish_norms(static_cast<int>(as ^ 1u), pre);
-                named_bar_sync(kConsumerBarrier, kConsumerThreads);
             }
 
             // Merge the column slices of each point: (score, index) order.
@@ -502,7 +522,7 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
             }
             const int row = w.row0 + lrow;
             if (ok && h == 0 && t < w.nsub && row < p.N) {
-                if (p.keys == nullptr) {
+                if (!w.split) {
                     float ms;
                     int ix;
                     if (bi == kNone) {
@@ -516,7 +536,7 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 2), 1)
                     if (p.minscore != nullptr)
                         p.minscore[row] = ms;
                 } else if (bi != kNone) {
-                    atomicMin(p.keys + row, pack_key(best, bi));
+                    atomicMin(p.keys + (row - p.split_row0 * SUB * kTileM), pack_key(best, bi));
                 }
             }
         }
@@ -541,7 +561,7 @@ template <int SUB, int NT, int CH, int KB>
 cudaError_t launch_one(const AssignParams &p, const CUtensorMap &xmap, const CUtensorMap &cmap,
                        int grid, size_t smem, cudaStream_t stream)
 {
-    assign_kernel<SUB, NT, CH, KB><<<grid, 32 * (4 * SUB * CH + 2), smem, stream>>>(xmap, cmap, p);
+    assign_kernel<SUB, NT, CH, KB><<<grid, 32 * (4 * SUB * CH + 3), smem, stream>>>(xmap, cmap, p);
     return cudaGetLastError();
 }
 
@@ -577,17 +597,22 @@ cudaError_t dispatch(bool prepare, const Variant &v, int kb, const AssignParams 
         return dispatch_kb<1, 256, 2>(prepare, kb, p, xmap, cmap, grid, smem, stream);
     if (v.sub == 2 && v.nt == 128 && v.ch == 1)
         return dispatch_kb<2, 128, 1>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+    if (v.sub == 2 && v.nt == 128 && v.ch == 2)
+        return dispatch_kb<2, 128, 2>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+    if (v.sub == 1 && v.nt == 256 && v.ch == 4)
+        return dispatch_kb<1, 256, 4>(prepare, kb, p, xmap, cmap, grid, smem, stream);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-const Variant kVariants[kNumVariants] = {{2, 128, 1}, {1, 256, 2}, {1, 128, 1}};
+const Variant kVariants[kNumVariants] = {{2, 128, 1}, {1, 256, 2}, {1, 128, 1}, {2, 128, 2},
+                                         {1, 256, 4}};
 
 size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 {
     return 1024 + static_cast<size_t>(xbufs) * v.sub * kblocks * kXTileBytes +
-           static_cast<size_t>(stages) * v.nt * 128 + 2 * v.nt * 4 +
+           static_cast<size_t>(stages) * v.nt * 128 + kCnStages * v.nt * 4 +
            static_cast<size_t>(v.ch - 1) * v.sub * kTileM * 8 + kMiscBytes;
 }
 

@@ -20,15 +20,17 @@ struct AssignParams {
     const float *cnorm;            // [K] fp32
     int32_t *idx;                  // [N] (direct store when ksplit == 1)
     float *minscore;               // [N] or nullptr (direct store when ksplit == 1)
-    unsigned long long *keys;      // [N] packed keys (ksplit > 1), else nullptr
+    unsigned long long *keys;      // packed keys of the split rows (row - split_row0 * rows per tile)
     int32_t N, K, D;
     int32_t ksteps;                // D / 16 tensor-core k-steps
     int32_t kblocks;               // ceil(D / 64) swizzled k-blocks
     int32_t rowtiles;              // ceil(N / (128 * sub))
-    int32_t ksplit;                // centroid ranges per row tile
+    int32_t full_units;            // row tiles [0, full_units) form one unit each, all of K
+    int32_t split_row0;            // row tiles [split_row0, rowtiles) are split over K
+    int32_t ksplit;                // centroid ranges per split row tile
     int32_t chunk_tiles;           // centroid tiles per range
     int32_t ntiles;                // ceil(K / nt)
-    int32_t num_units;             // rowtiles * ksplit
+    int32_t num_units;             // full_units + (rowtiles - split_row0) * ksplit
     int32_t stages;                // shared-memory ring depth
     int32_t xbufs;                 // X tile buffers (1 or 2)
     uint64_t timeout_ns;           // bound on every pipeline wait
@@ -40,7 +42,7 @@ struct AssignParams {
 struct Variant {
     int sub, nt, ch;
 };
-constexpr int kNumVariants = 3;
+constexpr int kNumVariants = 5;
 extern const Variant kVariants[kNumVariants];
 
 size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs);

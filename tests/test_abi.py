@@ -92,10 +92,11 @@ def test_null_and_alignment_errors(lib):
 def test_plan_value_errors(lib):
     S = km.STATUS
     ex = lib.kmassign_ex
-    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, -1, 0, 0, NULL) == S["KMASSIGN_ERR_ARG"]
-    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 64, 0, NULL) == S["KMASSIGN_ERR_ARG"]
-    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 0, 96, NULL) == S["KMASSIGN_ERR_ARG"]
-    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 256, 256, NULL) == S["KMASSIGN_ERR_ARG"]
+    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, -1, 0, 0, 0, NULL) == S["KMASSIGN_ERR_ARG"]
+    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 64, 0, 0, NULL) == S["KMASSIGN_ERR_ARG"]
+    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 0, 96, 0, NULL) == S["KMASSIGN_ERR_ARG"]
+    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 256, 256, 0, NULL) == S["KMASSIGN_ERR_ARG"]
+    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 0, 0, 12, NULL) == S["KMASSIGN_ERR_ARG"]
 
 
 def test_norms_argument_errors(lib):
@@ -112,7 +113,6 @@ def test_plan_rejects_null_output(lib):
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
-    import importlib
     import means_nearest_centroid_gb300 as mod
     saved = mod._lib
     try:
@@ -121,4 +121,3 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mod.library(str(tmp_path / "missing.so"))
     finally:
         mod._lib = saved
-    importlib.reload  # keep the module object as it was

@@ -22,6 +22,9 @@ PLANS = [
     dict(ksplit=3, rows_per_cta=256, centroids_per_tile=128),
     dict(ksplit=2, rows_per_cta=128, centroids_per_tile=256),
     dict(ksplit=5, rows_per_cta=128, centroids_per_tile=128),
+    dict(ksplit=-2, rows_per_cta=256, centroids_per_tile=128),
+    dict(rows_per_cta=256, centroids_per_tile=128, consumer_warps=16),
+    dict(ksplit=2, rows_per_cta=128, centroids_per_tile=256, consumer_warps=16),
 ]
 
 
@@ -215,3 +218,43 @@ def test_full_size_workloads(dev, key):
         assert bool((idx[finite] < w.K // 2).all())
         nan_rows = torch.isnan(X.float()).any(1)
         assert bool((idx[nan_rows] == 0).all()) and bool(torch.isnan(ms[nan_rows]).all())
+
+
+# ---------------------------------------------------------------- wave-tail split
+# More row tiles than thread blocks: the tail split keeps the first full waves
+# whole and splits only the last, partial wave (on a 152-SM GB300: 152 whole
+# row tiles, 5 split).
+TAIL_CASES = [
+    (20000, 700, 64, dict(ksplit=-2, rows_per_cta=128, centroids_per_tile=128)),
+    (20000, 700, 64, dict(ksplit=-3, rows_per_cta=128, centroids_per_tile=256)),
+    (40000, 300, 32, dict(ksplit=-2, rows_per_cta=256, centroids_per_tile=128)),
+    (40000, 1000, 48, dict(ksplit=-4, rows_per_cta=256, centroids_per_tile=128)),
+    (40000, 1000, 48, dict(ksplit=-3, rows_per_cta=256, centroids_per_tile=128,
+                           consumer_warps=16)),
+    (20000, 700, 64, dict(ksplit=-2, rows_per_cta=128, centroids_per_tile=256,
+                          consumer_warps=16)),
+]
+
+
+@pytest.mark.parametrize("N,K,D,plan", TAIL_CASES, ids=str)
+def test_tail_split_matches_oracle_and_whole_plan(dev, N, K, D, plan):
+    X, C = workloads.blobs(N, K, D, seed=N + K)
+    idx, ms = run(dev, X, C, plan=plan)
+    whole = dict(plan, ksplit=1)
+    idx1, ms1 = run(dev, X, C, plan=whole)
+    assert torch.equal(idx, idx1)
+    assert torch.equal(ms.view(torch.int32), ms1.view(torch.int32))
+    g = np.random.default_rng(N)
+    rows = np.unique(np.concatenate([g.choice(N, 3000, replace=False), np.arange(N - 2000, N)]))
+    rep = parity.compare(X, C, idx, ms, rows=rows)
+    assert rep.ok(), rep
+    Xi, Ci = workloads.integers(N, K, D, seed=N - K)
+    idx, ms = run(dev, Xi, Ci, plan=plan)
+    rep = parity.compare(Xi, Ci, idx, ms, rows=rows, integer=True)
+    assert rep.ok() and rep.idx_mismatches == 0, rep
+
+
+def test_invalid_tail_value_rejected(dev):
+    X, C = workloads.iid(10, 4, 64, seed=2)
+    with pytest.raises(km.KmassignError):
+        km.kmassign_ex(X.to(dev), C.to(dev), ksplit=-1)
