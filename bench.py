@@ -46,7 +46,7 @@ UNIT = "TFLOP/s"
 # results": N=262,144, D=256, K=16,384 in 1.8615 ms -> 1,181 TFLOP/s).
 PAGES_B200_TFLOPS = {"iid_normal": 2 * 262144 * 16384 * 256 / 1.8615e-3 / 1e12}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "assign_kernel_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "assign_kernel_traffic.txt")
 
 
 def log(*a):
@@ -71,10 +71,19 @@ def load_peaks():
 
 
 def load_traffic(kernel_sha: str):
+    """The ncu-measured DRAM bytes of one assign launch, if still current."""
+    t = {}
     try:
         with open(TRAFFIC_FILE) as f:
-            t = json.load(f)
-    except (OSError, ValueError):
+            for line in f:
+                if line.startswith("#") or ":" not in line:
+                    continue
+                k, v = line.split(":", 1)
+                v = v.strip()
+                t[k.strip()] = int(v) if v.isdigit() else v
+    except OSError:
+        return None, None
+    if not t:
         return None, None
     if t.get("source_sha") != kernel_sha:
         return None, t
