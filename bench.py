@@ -60,6 +60,20 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x (x itself without a process group)."""
+    if dist is None or not dist.is_initialized():
+        return float(x)
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_variants(rank: int, count: int = 3) -> list:
+    """Seed variants of the rotating input sets of one rank (disjoint across ranks)."""
+    return [count * int(rank) + v for v in range(count)]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -184,7 +198,7 @@ class ClockSampler:
 
 def make_inputs(key, variants, device, N=None, K=None, D=None):
     sets = []
-    for v in range(variants):
+    for v in variants:
         X, C = workloads.make(key, N=N, K=K, D=D, variant=v)
         sets.append((X, C))
     dev_sets = [(X.to(device), C.to(device)) for X, C in sets]
@@ -260,6 +274,63 @@ def run_reference(args, key):
     return 0
 
 
+# The 13 shapes of the pages' benchmark (flashlib PR #22, Performance and
+# "Benchmark results" tables) with their B200 latencies, context only.
+PAGES_SHAPES = [  # N, D, K, nightly ms, PR ms (B200)
+    (65536, 64, 512, 0.0727, 0.0441), (65536, 64, 4096, 0.1332, 0.1022),
+    (65536, 64, 16384, 0.3462, 0.2963), (65536, 128, 512, 0.0722, 0.0453),
+    (65536, 128, 4096, 0.1399, 0.1059), (262144, 128, 4096, 0.3444, 0.2844),
+    (262144, 128, 16384, 1.1653, 1.0047), (1048576, 128, 4096, 1.1978, 1.0148),
+    (65536, 256, 512, 0.0871, 0.0587), (65536, 256, 4096, 0.2111, 0.1661),
+    (262144, 256, 4096, 0.5640, 0.4631), (262144, 256, 16384, 2.0881, 1.8615),
+    (1048576, 256, 4096, 2.1431, 1.9458),
+]
+
+
+def run_pages_shapes(device):
+    """The pages' 13 shapes on this GPU, their method: three seeded bf16 sets
+    (17, 29, 43) rotated between calls, 10 warm-up and 30 timed calls, CUDA
+    events, median.  iid N(0,1) inputs (the pages give no distribution); norms
+    precomputed, so the time is the assignment call.  One JSON line each."""
+    import means_nearest_centroid_gb300 as km
+    stream = torch.cuda.current_stream(device)
+    rows = []
+    for N, D, K, nightly, pr in PAGES_SHAPES:
+        sets = []
+        for seed in (17, 29, 43):
+            X, C = workloads.iid(N, K, D, seed)
+            Xd, Cd = X.to(device), C.to(device)
+            sets.append((Xd, Cd, km.kmassign_norms(Cd, stream=stream),
+                         torch.empty(N, dtype=torch.int32, device=device)))
+        for i in range(10):
+            Xd, Cd, cn, idx = sets[i % 3]
+            km.kmassign(Xd, Cd, cnorm=cn, idx=idx, stream=stream)
+        times = []
+        for i in range(30):
+            Xd, Cd, cn, idx = sets[i % 3]
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            km.kmassign(Xd, Cd, cnorm=cn, idx=idx, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        rc = km.kmassign_check(stream)
+        ms = statistics.median(times)
+        line = {"N": N, "D": D, "K": K, "ms": ms, "tflops": 2.0 * N * K * D / ms / 1e9,
+                "b200_pr_ms": pr, "b200_nightly_ms": nightly, "status": rc,
+                "plan": km.kmassign_plan(N, K, D)}
+        rows.append(line)
+        print(json.dumps(line), flush=True)
+        del sets
+    geo = statistics.geometric_mean([r["ms"] for r in rows])
+    print(json.dumps({"geomean_ms": geo,
+                      "b200_pr_geomean_ms": statistics.geometric_mean([r[4] for r in PAGES_SHAPES]),
+                      "b200_nightly_geomean_ms": statistics.geometric_mean([r[3] for r in PAGES_SHAPES])}),
+          flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -271,6 +342,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-budget-s", type=float, default=150.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pages-shapes", action="store_true",
+                    help="time the pages' 13 benchmark shapes instead (context table)")
     ap.add_argument("--parity-rows", type=int, default=256)
     ap.add_argument("--N", type=int, default=None, help="override the workload's N")
     ap.add_argument("--K", type=int, default=None, help="override the workload's K")
@@ -287,6 +360,10 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    if args.pages_shapes:
+        from means_nearest_centroid_gb300 import _build
+        _build.build()
+        return run_pages_shapes(device)
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
@@ -307,7 +384,7 @@ def main():
     K = w.K if args.K is None else args.K
     resized = (N, D, K) != (w.N, w.D, w.K)
     flops = 2.0 * N * K * D
-    sets, dsets = make_inputs(key, 3, device, N, K, D)
+    sets, dsets = make_inputs(key, rank_variants(rank), device, N, K, D)
     cns = [torch.empty(K, dtype=torch.float32, device=device) for _ in dsets]
     idxs = [torch.empty(N, dtype=torch.int32, device=device) for _ in dsets]
     stream = torch.cuda.current_stream(device)
@@ -358,10 +435,7 @@ def main():
     sampler.stop()
     total_ms = t_start.elapsed_time(t_stop)
     kern_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, device)
     ms_per_step = total_ms / args.steps
     value = flops * ws * args.steps / (total_ms * 1e-3) / 1e12
 
@@ -418,11 +492,7 @@ def main():
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
             km.assign_host(Xh, Ch, idx_h, device=device, scratch=scratch)
-        e2e_s = time.perf_counter() - t0
-        if dist is not None:
-            t = torch.tensor([e2e_s], device=device, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(time.perf_counter() - t0, dist, device)
         e2e = {"value": flops * ws * args.e2e_steps / e2e_s / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": Xh.numel() * 2 + Ch.numel() * 2,
                "d2h_bytes_per_step": idx_h.numel() * 4, "steps": args.e2e_steps,

@@ -29,8 +29,9 @@
  * Ownership: the caller owns every buffer it passes.  The library keeps no
  * pointer after a call returns.  Temporaries (the norm buffer when cnorm is
  * NULL, and the packed-key workspace when the centroid range is split across
- * thread blocks) are taken with cudaMallocAsync and released with
- * cudaFreeAsync on the caller's stream.
+ * thread blocks) are stream-ordered allocations on the caller's stream from a
+ * memory pool the library creates per device; the pool keeps up to 1 GiB
+ * reserved between calls so that repeated calls do not re-map memory.
  *
  * Execution: every call is asynchronous on `stream` (a cudaStream_t passed as
  * void*; NULL is the legacy default stream) and never synchronises the host.
@@ -154,6 +155,15 @@ int kmassign_check(void *stream);
  */
 int kmassign_noalloc(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
                      int64_t D, int32_t *idx, float *minscore, void *stream);
+
+/*
+ * Bound, in nanoseconds of the GPU's global timer, on every pipeline wait in
+ * the kernels launched afterwards by this process (0 restores the default,
+ * 2 s).  A wait that runs out aborts its kernel cleanly and makes
+ * kmassign_check() return KMASSIGN_ERR_TIMEOUT; outputs are then undefined.
+ * Tests shrink it to make a timeout happen without faulting the GPU.
+ */
+int kmassign_set_wait_timeout(uint64_t ns);
 
 /* Static English text for a status code (never NULL). */
 const char *kmassign_strerror(int code);

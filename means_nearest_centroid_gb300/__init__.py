@@ -23,7 +23,7 @@ from . import _build
 
 __all__ = [
     "KmassignError", "library", "library_path", "kmassign", "kmassign_ex", "kmassign_norms",
-    "kmassign_noalloc",
+    "kmassign_noalloc", "kmassign_set_wait_timeout", "shard_rows",
     "kmassign_plan", "kmassign_check", "kmassign_strerror", "assign", "norms", "assign_host",
     "STATUS",
 ]
@@ -68,6 +68,8 @@ def _declare(lib):
     lib.kmassign_noalloc.restype = i32
     lib.kmassign_plan.argtypes = [i64, i64, i64, vp]
     lib.kmassign_plan.restype = i32
+    lib.kmassign_set_wait_timeout.argtypes = [ctypes.c_uint64]
+    lib.kmassign_set_wait_timeout.restype = i32
     lib.kmassign_check.argtypes = [vp]
     lib.kmassign_check.restype = i32
     lib.kmassign_strerror.argtypes = [i32]
@@ -212,6 +214,24 @@ def kmassign_plan(N: int, K: int, D: int) -> dict:
     keys = ["ksplit", "rows_per_cta", "centroids_per_tile", "grid", "stages", "xbufs",
             "whole_row_tiles", "split_row_tiles", "consumer_warps"]
     return dict(zip(keys, list(out)))
+
+
+def kmassign_set_wait_timeout(ns: int) -> None:
+    """Bound on every kernel pipeline wait, in ns (0 = default 2 s)."""
+    _check(library().kmassign_set_wait_timeout(int(ns)), "kmassign_set_wait_timeout")
+
+
+def shard_rows(N: int, rank: int, world: int) -> tuple:
+    """Contiguous, balanced share [begin, end) of N points for one of `world` GPUs.
+
+    The assignment needs no exchange between GPUs: each holds all centroids
+    and assigns its own rows; the answers concatenate in rank order.
+    """
+    if world < 1 or not 0 <= rank < world or N < 0:
+        raise ValueError("need N >= 0 and 0 <= rank < world")
+    base, extra = divmod(int(N), int(world))
+    begin = rank * base + min(rank, extra)
+    return begin, begin + base + (1 if rank < extra else 0)
 
 
 def kmassign_check(stream=None) -> int:

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -15,12 +16,18 @@ using kma::AssignParams;
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
 constexpr int kMaxDevices = 64;
+std::atomic<uint64_t> g_wait_timeout_ns{kDefaultTimeoutNs};
 
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int smem_optin = 0;
+    // Library-owned stream-ordered pool for the temporaries.  It keeps up to
+    // kPoolKeepBytes reserved across synchronisations; the default pool would
+    // hand its memory back at every synchronisation and re-map it per call.
+    cudaMemPool_t pool = nullptr;
 };
+constexpr uint64_t kPoolKeepBytes = uint64_t(1) << 30;
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
@@ -43,6 +50,14 @@ int current_device_info(DeviceInfo *out)
             for (int kb = 1; kb <= 4; ++kb)
                 if (kma::assign_prepare(v, kb, static_cast<size_t>(d.smem_optin)) != cudaSuccess)
                     return KMASSIGN_ERR_CUDA;
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        uint64_t keep = kPoolKeepBytes;
+        if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess ||
+            cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
+            return KMASSIGN_ERR_CUDA;
         d.ready = true;
     }
     *out = d;
@@ -205,8 +220,13 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
             const int64_t full_units = any_split ? F : R;   // ks 1: nothing is split
             const int64_t split_row0 = any_split ? F : R;
             const int64_t nunits = full_units + (R - split_row0) * (any_split ? ks_eff : 1);
+            // A block's load is piecewise constant in its index, changing
+            // only where the whole and the split ranges end.
             double worst = 0.0;
-            for (int64_t b = 0; b < std::min<int64_t>(P, nunits); ++b) {
+            const int64_t probes[4] = {0, full_units % P, nunits % P, P - 1};
+            for (int64_t b : probes) {
+                if (b >= std::min<int64_t>(P, nunits))
+                    continue;
                 const int64_t nf = units_of_block(full_units, P, b);
                 const int64_t ns = units_of_block(nunits, P, b) - nf;
                 const double c = double(nf) * (double(ntiles) * tile + unit_over) +
@@ -255,6 +275,44 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
     return KMASSIGN_OK;
 }
 
+// Plans are pure functions of (shape, forced fields, device): remember them.
+struct PlanKey {
+    int64_t N, K, D;
+    int ksplit, rows, nt, cw, dev;
+    bool operator==(const PlanKey &o) const
+    {
+        return N == o.N && K == o.K && D == o.D && ksplit == o.ksplit && rows == o.rows &&
+               nt == o.nt && cw == o.cw && dev == o.dev;
+    }
+};
+constexpr int kPlanCacheSize = 64;
+PlanKey g_plan_keys[kPlanCacheSize];
+Plan g_plans[kPlanCacheSize];
+int g_plan_count = 0, g_plan_next = 0;
+
+int cached_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int dev_id, int ksplit,
+                int rows, int nt, int cw, Plan *out)
+{
+    const PlanKey key{N, K, D, ksplit, rows, nt, cw, dev_id};
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        for (int i = 0; i < g_plan_count; ++i)
+            if (g_plan_keys[i] == key) {
+                *out = g_plans[i];
+                return KMASSIGN_OK;
+            }
+    }
+    const int rc = make_plan(N, K, D, dev, ksplit, rows, nt, cw, out);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_plan_keys[g_plan_next] = key;
+    g_plans[g_plan_next] = *out;
+    g_plan_next = (g_plan_next + 1) % kPlanCacheSize;
+    g_plan_count = std::min(g_plan_count + 1, kPlanCacheSize);
+    return KMASSIGN_OK;
+}
+
 // Fill the kernel parameters of a plan.
 AssignParams make_params(const Plan &plan, const float *cnorm, int32_t *idx, float *minscore,
                          unsigned long long *keys, int64_t N, int64_t K, int64_t D)
@@ -278,7 +336,7 @@ AssignParams make_params(const Plan &plan, const float *cnorm, int32_t *idx, flo
     p.num_units = plan.units;
     p.stages = plan.stages;
     p.xbufs = plan.xbufs;
-    p.timeout_ns = kDefaultTimeoutNs;
+    p.timeout_ns = g_wait_timeout_ns.load();
     return p;
 }
 
@@ -311,9 +369,11 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
     DeviceInfo dev;
     if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
     Plan plan;
-    if ((rc = make_plan(N, K, D, dev, force_ksplit, force_rows, force_nt, force_cw, &plan)) !=
-        KMASSIGN_OK)
+    if ((rc = cached_plan(N, K, D, dev, dev_id, force_ksplit, force_rows, force_nt, force_cw,
+                          &plan)) != KMASSIGN_OK)
         return rc;
 
     CUtensorMap xmap, cmap;
@@ -326,8 +386,8 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
     unsigned long long *keys = nullptr;
     rc = KMASSIGN_OK;
     if (cnorm == nullptr) {
-        if (cudaMallocAsync(reinterpret_cast<void **>(&tmp_norm), static_cast<size_t>(K) * 4,
-                            stream) != cudaSuccess)
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&tmp_norm),
+                                    static_cast<size_t>(K) * 4, dev.pool, stream) != cudaSuccess)
             return KMASSIGN_ERR_CUDA;
         if (kma::launch_norms(C, K, D, tmp_norm, stream) != cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
@@ -336,8 +396,9 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
     const int64_t row_split = split_first_row(plan);
     const int64_t n_split = plan.ksplit > 1 ? N - row_split : 0;
     if (rc == KMASSIGN_OK && n_split > 0) {
-        if (cudaMallocAsync(reinterpret_cast<void **>(&keys), static_cast<size_t>(n_split) * 8,
-                            stream) != cudaSuccess ||
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&keys),
+                                    static_cast<size_t>(n_split) * 8, dev.pool,
+                                    stream) != cudaSuccess ||
             cudaMemsetAsync(keys, 0xff, static_cast<size_t>(n_split) * 8, stream) != cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
     }
@@ -534,6 +595,12 @@ int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9)
     out9[6] = plan.full_units;
     out9[7] = plan.rowtiles - plan.split_row0;
     out9[8] = 4 * plan.v.sub * plan.v.ch;
+    return KMASSIGN_OK;
+}
+
+int kmassign_set_wait_timeout(uint64_t ns)
+{
+    g_wait_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
     return KMASSIGN_OK;
 }
 

@@ -7,10 +7,12 @@
 // selected with lowest-index tie breaking.
 //
 // Roles inside one thread block (one block per SM, persistent):
-//   * producer warp  - TMA-loads the block's X tile once per work unit (the
+//   * X warp         - TMA-loads the block's X tile once per work unit (the
 //                      tile stays resident while centroids stream past it)
-//                      and streams C k-blocks through a ring of shared-memory
-//                      stages guarded by full/empty mbarriers;
+//                      and asks L2 to prefetch the next unit's X tile;
+//   * producer warp  - streams C k-blocks through a ring of shared-memory
+//                      stages guarded by full/empty mbarriers, straight across
+//                      unit boundaries;
 //   * MMA warp       - converged, one elected lane issues tcgen05.mma (bf16
 //                      in, fp32 out) into one of two tensor-memory accumulator
 //                      stages; the k-loop is unrolled at compile time with the
@@ -34,7 +36,12 @@
 // chunk (two lanes per packed fma), the chunk minimum by a 3-input min tree
 // (NaN ignored) -- four chunks at a time so their dependency chains overlap --
 // and only when a chunk minimum beats the running best is the first column
-// holding it searched.  Chunks are visited in increasing centroid order, so a
+// holding it located.  The whole warp pays for that step whenever any of its
+// lanes improves, which early in a scan is nearly every chunk, so for D <= 128
+// (where the reduction, not the tensor pipe, bounds the kernel) an improving
+// lane only stores its chunk's 32 scores to its own shared-memory slot and
+// the position is found once, when the unit ends; for larger D the lane
+// searches at once.  Chunks are visited in increasing centroid order, so a
 // warp keeps the lowest index on ties; column slices and split centroid
 // ranges merge by (score, index).  A NaN score never wins.
 //
@@ -77,6 +84,9 @@ constexpr int kBarCnEmpty = kBarCnFull + kCnStages;   // [kCnStages]
 constexpr int kNumBars = kBarCnEmpty + kCnStages;
 constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot + abort flag
 constexpr uint32_t kConsumerBarrier = 1;              // named barrier id
+// Bound on the teardown waits after an abort (copies and MMAs in flight
+// always finish; this only guards against a hardware failure).
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 __device__ __forceinline__ void record_timeout()
 {
@@ -209,22 +219,56 @@ __device__ __forceinline__ void apply_norms(float (&v)[32], uint32_t cn_addr)
     }
 }
 
+// First position of m in s (m is the minimum of s, so one exists).
+__device__ __forceinline__ int first_of(const float (&s)[32], float m)
+{
+    int pos = 31;
+#pragma unroll
+    for (int i = 30; i >= 0; --i)
+        pos = (s[i] == m) ? i : pos;
+    return pos;
+}
+
 // Fold chunk scores s (columns j0 .. j0+31, chunk minimum m) into (best, bi).
+// SNAP: keep the chunk's scores in this thread's shared slot (float4 i of
+// thread t at slot + 512*i, conflict-free across the warp) and let bi hold the
+// chunk's first column until resolve_snapshot.
+template <bool SNAP>
 __device__ __forceinline__ void fold_chunk(const float (&s)[32], float m, int j0, float &best,
-                                           int &bi)
+                                           int &bi, uint32_t slot)
 {
     if (m < best || (m == best && bi == kNone)) {
-        int pos = 31;
-#pragma unroll
-        for (int i = 30; i >= 0; --i)
-            pos = (s[i] == m) ? i : pos;
         best = m;
-        bi = j0 + pos;
+        if (SNAP) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                st_shared_v4(slot + 512u * i, s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+            bi = j0;
+        } else {
+            bi = j0 + first_of(s, m);
+        }
     }
 }
 
+// Turn a snapshot's chunk start into the winning column.
+__device__ __forceinline__ void resolve_snapshot(float best, int &bi, uint32_t slot)
+{
+    if (bi == kNone)
+        return;
+    float s[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 q = ld_shared_v4(slot + 512u * i);
+        s[4 * i] = q.x;
+        s[4 * i + 1] = q.y;
+        s[4 * i + 2] = q.z;
+        s[4 * i + 3] = q.w;
+    }
+    bi += first_of(s, best);
+}
+
 template <int SUB, int NT, int CH, int KB>
-__global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
+__global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     assign_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap cmap,
                   const AssignParams p)
 {
@@ -233,6 +277,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
     constexpr int kProducerWarp = kConsumerWarps;
     constexpr int kMmaWarp = kConsumerWarps + 1;
     constexpr int kNormWarp = kConsumerWarps + 2;
+    constexpr int kXWarp = kConsumerWarps + 3;
+    constexpr bool kSnap = KB <= 2;                    // D <= 128: epilogue-bound
     constexpr int kCW = NT / CH;                       // columns per consumer warp per tile
     constexpr int kChunks = kCW / 32;
     constexpr int kGroup = kChunks < 4 ? kChunks : 4;  // chunks loaded per tcgen05.wait::ld
@@ -252,7 +298,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
     const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
     const uint32_t cn_base = c_base + p.stages * kCStageBytes;       // float[kCnStages][NT]
     const uint32_t red_base = cn_base + kCnStages * NT * 4;           // {float,int}[CH-1][SUB*128]
-    const uint32_t bar_base = red_base + (CH - 1) * SUB * kTileM * 8;
+    const uint32_t snap_base = red_base + (CH - 1) * SUB * kTileM * 8;   // [warp][8][32] float4
+    const uint32_t bar_base = snap_base + (kSnap ? kConsumerWarps * 4096u : 0u);
     uint8_t *const sbase = smem_raw + (base - raw);
     uint8_t *misc_ptr = smem_raw + (bar_base - raw) + kNumBars * 8;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(misc_ptr);
@@ -296,25 +343,12 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
         if (lane == 0) {
             tma_prefetch_desc(&xmap);
             tma_prefetch_desc(&cmap);
-            const uint64_t pol_x = policy_evict_first();
             const uint64_t pol_c = policy_evict_last();
             uint32_t stage = 0, phase = 0;
-            uint32_t c_issued = 0, x_issued = 0;
+            uint32_t c_issued = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
                 const Unit w = decode_unit<SUB>(p, u);
-                const uint32_t xb = x_issued % p.xbufs;
-                const uint32_t xph = (x_issued / p.xbufs) & 1u;
-                if (!(ok = wait1(bar(kBarXEmpty + xb), xph ^ 1u, abort_flag, p.timeout_ns)))
-                    break;
-                mbar_arrive_expect_tx(bar(kBarXFull + xb), w.nsub * KB * kXTileBytes);
-                const uint32_t xdst = x_base + xb * kXBufBytes;
-                for (int t = 0; t < w.nsub; ++t)
-#pragma unroll
-                    for (int kb = 0; kb < KB; ++kb)
-                        tma_load_2d(xdst + (t * KB + kb) * kXTileBytes, &xmap, bar(kBarXFull + xb),
-                                    kb * kKBlock, w.row0 + t * kTileM, pol_x);
-                ++x_issued;
                 for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb) {
@@ -336,10 +370,44 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
                 // Let every copy still in flight land before the block exits.
                 const uint32_t S = p.stages;
                 for (uint32_t n = (c_issued > S ? c_issued - S : 0); n < c_issued; ++n)
-                    wait1(bar(kBarCFull + n % S), (n / S) & 1u, abort_flag, p.timeout_ns, false);
+                    wait1(bar(kBarCFull + n % S), (n / S) & 1u, abort_flag, kDrainLimitNs, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kXWarp) {
+        if (lane == 0) {
+            const uint64_t pol_x = policy_evict_first();
+            uint32_t x_issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = decode_unit<SUB>(p, u);
+                const uint32_t xb = x_issued % p.xbufs;
+                const uint32_t xph = (x_issued / p.xbufs) & 1u;
+                if (!(ok = wait1(bar(kBarXEmpty + xb), xph ^ 1u, abort_flag, p.timeout_ns)))
+                    break;
+                mbar_arrive_expect_tx(bar(kBarXFull + xb), w.nsub * KB * kXTileBytes);
+                const uint32_t xdst = x_base + xb * kXBufBytes;
+                for (int t = 0; t < w.nsub; ++t)
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_load_2d(xdst + (t * KB + kb) * kXTileBytes, &xmap, bar(kBarXFull + xb),
+                                    kb * kKBlock, w.row0 + t * kTileM, pol_x);
+                ++x_issued;
+                // The next unit's tile comes from L2 when its buffer frees up.
+                const int un = u + static_cast<int>(gridDim.x);
+                if (un < p.num_units) {
+                    const Unit wn = decode_unit<SUB>(p, un);
+                    if (wn.row0 != w.row0)
+                        for (int t = 0; t < wn.nsub; ++t)
+#pragma unroll
+                            for (int kb = 0; kb < KB; ++kb)
+                                tma_prefetch_l2_2d(&xmap, kb * kKBlock, wn.row0 + t * kTileM);
+                }
+            }
+            if (!ok) {
                 const uint32_t B = p.xbufs;
                 for (uint32_t n = (x_issued > B ? x_issued - B : 0); n < x_issued; ++n)
-                    wait1(bar(kBarXFull + n % B), (n / B) & 1u, abort_flag, p.timeout_ns, false);
+                    wait1(bar(kBarXFull + n % B), (n / B) & 1u, abort_flag, kDrainLimitNs, false);
             }
         }
         __syncwarp();
@@ -411,7 +479,7 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
             if (elect_one())
                 mma_commit(bar(kBarDrain));
             __syncwarp();
-            wait_warp(bar(kBarDrain), 0u, abort_flag, p.timeout_ns, false);
+            wait_warp(bar(kBarDrain), 0u, abort_flag, kDrainLimitNs, false);
         }
     } else if (warp == kNormWarp) {
         // Norm warp: one ring slot per tile of this block's schedule.
@@ -443,6 +511,7 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
         const int h = warp / (4 * SUB);
         const int col0 = h * kCW;
         const uint32_t cn_col = cn_base + 4u * static_cast<uint32_t>(col0);
+        const uint32_t slot = snap_base + 4096u * warp + 16u * lane;
         const float kNaN = __int_as_float(0x7fc00000);
         uint32_t acc_used = 0;
         bool ok = true;
@@ -489,7 +558,7 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
                         const int jg = tile * NT + col0 + g * kGroup * 32;
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c)
-                            fold_chunk(v[c], m[c], jg + 32 * c, best, bi);
+                            fold_chunk<kSnap>(v[c], m[c], jg + 32 * c, best, bi, slot);
                     }
                     // This warp is done with the tile's norms.
                     __syncwarp();
@@ -498,6 +567,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 3), 1)
                 }
             }
 
+            if (kSnap)
+                resolve_snapshot(best, bi, slot);
             // Merge the column slices of each point: (score, index) order.
             const int lrow = t * kTileM + q * 32 + lane;
             if (CH > 1) {
@@ -561,7 +632,7 @@ template <int SUB, int NT, int CH, int KB>
 cudaError_t launch_one(const AssignParams &p, const CUtensorMap &xmap, const CUtensorMap &cmap,
                        int grid, size_t smem, cudaStream_t stream)
 {
-    assign_kernel<SUB, NT, CH, KB><<<grid, 32 * (4 * SUB * CH + 3), smem, stream>>>(xmap, cmap, p);
+    assign_kernel<SUB, NT, CH, KB><<<grid, 32 * (4 * SUB * CH + 4), smem, stream>>>(xmap, cmap, p);
     return cudaGetLastError();
 }
 
@@ -613,7 +684,8 @@ size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 {
     return 1024 + static_cast<size_t>(xbufs) * v.sub * kblocks * kXTileBytes +
            static_cast<size_t>(stages) * v.nt * 128 + kCnStages * v.nt * 4 +
-           static_cast<size_t>(v.ch - 1) * v.sub * kTileM * 8 + kMiscBytes;
+           static_cast<size_t>(v.ch - 1) * v.sub * kTileM * 8 +
+           (kblocks <= 2 ? static_cast<size_t>(4 * v.sub * v.ch) * 4096 : 0) + kMiscBytes;
 }
 
 cudaError_t assign_prepare(const Variant &v, int kblocks, size_t smem)
