@@ -100,13 +100,15 @@ int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_
  *                       keys.  ksplit <= -2 splits only the row tiles of the
  *                       last, partial wave of thread blocks into -ksplit
  *                       ranges (wave-tail balancing); -1 is invalid
- *   rows_per_cta        128 or 256 points per thread block tile
- *   centroids_per_tile  128 or 256 centroids per tensor-core tile
- *                       (rows_per_cta 256 requires 128)
- *   consumer_warps      warps reducing the score tiles: 4 (128x128 tiles),
- *                       8 or 16 (128x256 and 256x128 tiles)
+ *   rows_per_cta        128 or 256 points per work unit
+ *   centroids_per_tile  128 or 256 centroids per tensor-core tile; 256 with
+ *                       256 rows selects the CTA-pair kernel (two thread
+ *                       blocks on two SMs share each 256x256 tile)
+ *   consumer_warps      warps reducing the score tiles per thread block: 4
+ *                       (128x128 tiles), 8 or 16 (all other shapes)
  * Same arguments, layout and errors as kmassign; a value outside these sets,
- * or a combination no compiled kernel has, returns KMASSIGN_ERR_ARG.  Tests
+ * or a combination no compiled kernel has (or no pair of SMs can run),
+ * returns KMASSIGN_ERR_ARG.  Tests
  * use it to cover every path.
  */
 int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,

@@ -26,6 +26,7 @@ struct DeviceInfo {
     // kPoolKeepBytes reserved across synchronisations; the default pool would
     // hand its memory back at every synchronisation and re-map it per call.
     cudaMemPool_t pool = nullptr;
+    int pair_clusters = 0;   // co-resident clusters of the pair kernel (0: none)
 };
 constexpr uint64_t kPoolKeepBytes = uint64_t(1) << 30;
 
@@ -54,6 +55,14 @@ int current_device_info(DeviceInfo *out)
         props.allocType = cudaMemAllocationTypePinned;
         props.location.type = cudaMemLocationTypeDevice;
         props.location.id = dev;
+        int clusters = 0;
+        const kma::Variant pv{1, 256, 2, true};
+        if (kma::assign_max_clusters(pv, 4, static_cast<size_t>(d.smem_optin), &clusters) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            clusters = 0;
+        }
+        d.pair_clusters = std::min(clusters, d.sms / 2);
         uint64_t keep = kPoolKeepBytes;
         if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess ||
             cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
@@ -179,19 +188,22 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
               int force_rows, int force_nt, int force_cw, Plan *out)
 {
     const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
-    const int64_t P = dev.sms;
     bool found = false;
     double best_cost = 0.0;
     Plan best{};
     for (const auto &v : kma::kVariants) {
-        if (force_rows != 0 && force_rows != v.sub * kma::kTileM)
+        const int rows = (v.pair ? 2 : v.sub) * kma::kTileM;   // points per unit
+        if (force_rows != 0 && force_rows != rows)
             continue;
         if (force_nt != 0 && force_nt != v.nt)
             continue;
         if (force_cw != 0 && force_cw != 4 * v.sub * v.ch)
             continue;
+        if (v.pair && dev.pair_clusters < 1)
+            continue;
+        const int64_t P = v.pair ? dev.pair_clusters : dev.sms;   // units run in parallel
         const size_t xbytes = static_cast<size_t>(v.sub) * kblocks * kma::kXTileBytes;
-        const size_t stage_bytes = static_cast<size_t>(v.nt) * 128;
+        const size_t stage_bytes = static_cast<size_t>(v.pair ? v.nt / 2 : v.nt) * 128;
         const size_t fixed = kma::assign_smem_bytes(v, kblocks, 0, 0);
         const size_t budget = static_cast<size_t>(dev.smem_optin);
         if (fixed + xbytes + 2 * stage_bytes > budget)
@@ -200,12 +212,15 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const int stages = static_cast<int>(std::min<size_t>(
             kma::kMaxStages, (budget - fixed - xbufs * xbytes) / stage_bytes));
         const int64_t ntiles = cdiv(K, v.nt);
-        const int64_t R = cdiv(N, static_cast<int64_t>(v.sub) * kma::kTileM);
+        const int64_t R = cdiv(N, static_cast<int64_t>(rows));
         const double mma_clk = v.nt == 256 ? 128.0 : (v.sub == 2 ? 80.0 : 92.0);
         const double tile_mma = double(v.sub) * kblocks * 4 * mma_clk + 500.0;
         const double tile_epi = v.nt == 256 ? 2150.0
                                 : v.sub == 2 ? (v.ch == 2 ? 1550.0 : 1700.0) : 1400.0;
-        const double tile = std::max(tile_mma, tile_epi);
+        // The pair kernel couples both SMs' consumers on every tile; measured
+        // ~20% slower than the single-block shapes, so it is only chosen when
+        // forced (kmassign_ex).
+        const double tile = std::max(tile_mma, tile_epi) * (v.pair ? 1.25 : 1.0);
         const double unit_over = 5000.0;
 
         // Candidate (F whole row tiles, split the rest into ks ranges).
@@ -245,7 +260,7 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
                 best.full_units = static_cast<int>(full_units);
                 best.split_row0 = static_cast<int>(split_row0);
                 best.units = static_cast<int>(nunits);
-                best.grid = static_cast<int>(std::min<int64_t>(nunits, P));
+                best.grid = static_cast<int>(std::min<int64_t>(nunits, P) * (v.pair ? 2 : 1));
                 best.stages = stages;
                 best.xbufs = xbufs;
                 best.smem = kma::assign_smem_bytes(v, kblocks, stages, xbufs);
@@ -340,8 +355,18 @@ AssignParams make_params(const Plan &plan, const float *cnorm, int32_t *idx, flo
     return p;
 }
 
-// First point whose answer goes through the packed keys, and their count.
-int64_t split_first_row(const Plan &plan) { return int64_t(plan.split_row0) * plan.v.sub * kma::kTileM; }
+// Rows of C in one TMA box: the whole tile, or each CTA's half of it when a
+// CTA pair shares the tile (each loads 128 of its 256 centroids).
+uint32_t c_box_rows(const Plan &plan)
+{
+    return static_cast<uint32_t>(plan.v.pair ? plan.v.nt / 2 : plan.v.nt);
+}
+
+// First point whose answer goes through the packed keys.
+int64_t split_first_row(const Plan &plan)
+{
+    return int64_t(plan.split_row0) * (plan.v.pair ? 2 : plan.v.sub) * kma::kTileM;
+}
 
 int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
                int32_t *idx, float *minscore, int force_ksplit, int force_rows, int force_nt,
@@ -352,7 +377,6 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
         return rc;
     if (force_ksplit == -1 || (force_rows != 0 && force_rows != 128 && force_rows != 256) ||
         (force_nt != 0 && force_nt != 128 && force_nt != 256) ||
-        (force_rows == 256 && force_nt == 256) ||
         (force_cw != 0 && force_cw != 4 && force_cw != 8 && force_cw != 16))
         return KMASSIGN_ERR_ARG;
     if (N == 0)
@@ -379,7 +403,7 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
     CUtensorMap xmap, cmap;
     if (!encode_map(&xmap, X, static_cast<uint64_t>(N), static_cast<uint64_t>(D), kma::kTileM) ||
         !encode_map(&cmap, C, static_cast<uint64_t>(K), static_cast<uint64_t>(D),
-                    static_cast<uint32_t>(plan.v.nt)))
+                    c_box_rows(plan)))
         return KMASSIGN_ERR_CUDA;
 
     float *tmp_norm = nullptr;
@@ -497,7 +521,7 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
     CUtensorMap xmap, cmap;
     if (!encode_map(&xmap, X, static_cast<uint64_t>(N), static_cast<uint64_t>(D), kma::kTileM) ||
         !encode_map(&cmap, C, static_cast<uint64_t>(K), static_cast<uint64_t>(D),
-                    static_cast<uint32_t>(plan.v.nt)))
+                    c_box_rows(plan)))
         return KMASSIGN_ERR_CUDA;
 
     unsigned char *scratch = nullptr;
@@ -587,7 +611,7 @@ int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9)
     if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, 0, 0, 0, 0, &plan)) != KMASSIGN_OK)
         return rc;
     out9[0] = plan.ksplit;
-    out9[1] = plan.v.sub * kma::kTileM;
+    out9[1] = (plan.v.pair ? 2 : plan.v.sub) * kma::kTileM;
     out9[2] = plan.v.nt;
     out9[3] = plan.grid;
     out9[4] = plan.stages;

@@ -621,6 +621,412 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant (cta_group::2): a cluster of two CTAs on two SMs computes
+// 256x256 tiles.  Each CTA keeps its own 128 X rows resident and loads only
+// its 128-row half of every C k-block (16 KiB instead of 32), so L2 traffic
+// per flop halves and the ring of stages reaches twice as far ahead for the
+// same shared memory.  The leader CTA (rank 0) issues the pair MMAs; their
+// completion is multicast to both CTAs' barriers; the peer's copies count on
+// the leader's full barriers and its consumers hand accumulator stages back
+// by arriving on the leader's empty barriers.  Everything else (norm ring,
+// reduction, stores) is per CTA and identical to the single-CTA kernel.
+template <int CH, int KB>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1)
+    assign_pair_kernel(const __grid_constant__ CUtensorMap xmap,
+                       const __grid_constant__ CUtensorMap cmap, const AssignParams p)
+{
+    constexpr int NT = 256;                            // centroids per pair tile
+    constexpr int kHalf = 128;                         // C rows each CTA loads
+    constexpr int kConsumerWarps = 4 * CH;
+    constexpr int kProducerWarp = kConsumerWarps;
+    constexpr int kMmaWarp = kConsumerWarps + 1;
+    constexpr int kNormWarp = kConsumerWarps + 2;
+    constexpr int kXWarp = kConsumerWarps + 3;
+    constexpr bool kSnap = KB <= 2;
+    constexpr int kCW = NT / CH;
+    constexpr int kChunks = kCW / 32;
+    constexpr int kGroup = kChunks < 4 ? kChunks : 4;
+    constexpr int kGroups = kChunks / kGroup;
+    constexpr uint32_t kCStageBytes = kHalf * 128;
+    constexpr uint32_t kXBufBytes = KB * kXTileBytes;
+    constexpr uint32_t kAccCols = NT;
+    constexpr uint32_t kTmemCols = 2 * kAccCols;
+    constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kTileM, NT);
+    constexpr uint16_t kBoth = 0x3;
+    static_assert(kCW % 32 == 0 && kChunks % kGroup == 0, "column slice must be whole chunks");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t x_base = base;
+    const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
+    const uint32_t cn_base = c_base + p.stages * kCStageBytes;
+    const uint32_t red_base = cn_base + kCnStages * NT * 4;
+    const uint32_t snap_base = red_base + (CH - 1) * kTileM * 8;
+    const uint32_t bar_base = snap_base + (kSnap ? kConsumerWarps * 4096u : 0u);
+    uint8_t *const sbase = smem_raw + (base - raw);
+    uint8_t *misc_ptr = smem_raw + (bar_base - raw) + kNumBars * 8;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(misc_ptr);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(misc_ptr + 4);
+    auto bar = [&](int i) -> uint32_t { return bar_base + 8u * static_cast<uint32_t>(i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    // The leader's copy of barrier i, as a cluster address.
+    auto lead_bar = [&](int i) -> uint32_t { return map_to_rank(bar(i), 0); };
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kMaxXBufs; ++b) {
+            mbar_init(bar(kBarXFull + b), 1);
+            mbar_init(bar(kBarXEmpty + b), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar(kBarAccFull + a), 1);
+            mbar_init(bar(kBarAccEmpty + a), 2 * kConsumerWarps);
+        }
+        mbar_init(bar(kBarDrain), 1);
+        for (int s = 0; s < kMaxStages; ++s) {
+            mbar_init(bar(kBarCFull + s), 1);
+            mbar_init(bar(kBarCEmpty + s), 1);
+        }
+        for (int s = 0; s < kCnStages; ++s) {
+            mbar_init(bar(kBarCnFull + s), 32);
+            mbar_init(bar(kBarCnEmpty + s), kConsumerWarps);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc_pair(smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers exist before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int cluster = static_cast<int>(blockIdx.x >> 1);
+    const int nclusters = static_cast<int>(gridDim.x >> 1);
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            tma_prefetch_desc(&cmap);
+            const uint64_t pol_c = policy_evict_last();
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+                const Unit w = decode_unit<2>(p, u);
+                for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) {
+                        if (!(ok = wait1(bar(kBarCEmpty + stage), phase ^ 1u, abort_flag,
+                                         p.timeout_ns)))
+                            break;
+                        if (leader)
+                            mbar_arrive_expect_tx(bar(kBarCFull + stage), 2 * kCStageBytes);
+                        tma_load_2d_pair(c_base + stage * kCStageBytes, &cmap,
+                                         lead_bar(kBarCFull + stage), kb * kKBlock,
+                                         tile * NT + static_cast<int>(rank) * kHalf, pol_c);
+                        if (++stage == static_cast<uint32_t>(p.stages)) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                // Copies in flight complete on the leader's barriers, out of
+                // this CTA's sight: give them time to land (they take
+                // microseconds) before the block can exit.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 1000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kXWarp) {
+        if (lane == 0) {
+            tma_prefetch_desc(&xmap);
+            const uint64_t pol_x = policy_evict_first();
+            uint32_t x_issued = 0;
+            bool ok = true;
+            for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+                const Unit w = decode_unit<2>(p, u);
+                const uint32_t xb = x_issued % p.xbufs;
+                const uint32_t xph = (x_issued / p.xbufs) & 1u;
+                if (!(ok = wait1(bar(kBarXEmpty + xb), xph ^ 1u, abort_flag, p.timeout_ns)))
+                    break;
+                // The leader's barrier counts both CTAs' rows (the peer's only
+                // when its 128 rows hold points).
+                if (leader)
+                    mbar_arrive_expect_tx(bar(kBarXFull + xb), w.nsub * KB * kXTileBytes);
+                if (static_cast<int>(rank) < w.nsub) {
+                    const uint32_t xdst = x_base + xb * kXBufBytes;
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_load_2d_pair(xdst + kb * kXTileBytes, &xmap, lead_bar(kBarXFull + xb),
+                                         kb * kKBlock, w.row0 + static_cast<int>(rank) * kTileM,
+                                         pol_x);
+                }
+                ++x_issued;
+                const int un = u + nclusters;
+                if (un < p.num_units) {
+                    const Unit wn = decode_unit<2>(p, un);
+                    if (wn.row0 != w.row0 && static_cast<int>(rank) < wn.nsub)
+#pragma unroll
+                        for (int kb = 0; kb < KB; ++kb)
+                            tma_prefetch_l2_2d(&xmap, kb * kKBlock,
+                                               wn.row0 + static_cast<int>(rank) * kTileM);
+                }
+            }
+            if (!ok) {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 1000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (leader) {
+            uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0;
+            bool ok = true, issued = false;
+            for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+                const Unit w = decode_unit<2>(p, u);
+                const uint32_t xb = x_used % p.xbufs;
+                const uint32_t xph = (x_used / p.xbufs) & 1u;
+                if (!(ok = wait_warp(bar(kBarXFull + xb), xph, abort_flag, p.timeout_ns)))
+                    break;
+                uint64_t adesc[KB];
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+                    adesc[kb] = sw128_kmajor_desc(x_base + xb * kXBufBytes + kb * kXTileBytes);
+                for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
+                    const uint32_t as = acc_used & 1u;
+                    const uint32_t aph = (acc_used >> 1) & 1u;
+                    if (!(ok = wait_warp(bar(kBarAccEmpty + as), aph ^ 1u, abort_flag,
+                                         p.timeout_ns)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + as * kAccCols;
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) {
+                        if (!(ok = wait_warp(bar(kBarCFull + stage), phase, abort_flag,
+                                             p.timeout_ns)))
+                            break;
+                        const uint64_t cdesc = sw128_kmajor_desc(c_base + stage * kCStageBytes);
+                        if (elect_one()) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_bf16_pair(d_tmem, adesc[kb] + 2u * k, cdesc + 2u * k, kIdesc,
+                                              (kb | k) != 0);
+                            mma_commit_pair(bar(kBarCEmpty + stage), kBoth);
+                        }
+                        __syncwarp();
+                        issued = true;
+                        if (++stage == static_cast<uint32_t>(p.stages)) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    if (elect_one())
+                        mma_commit_pair(bar(kBarAccFull + as), kBoth);
+                    __syncwarp();
+                    ++acc_used;
+                }
+                if (!ok)
+                    break;
+                if (elect_one())
+                    mma_commit_pair(bar(kBarXEmpty + xb), kBoth);
+                __syncwarp();
+                ++x_used;
+            }
+            if (issued) {
+                if (elect_one())
+                    mma_commit_pair(bar(kBarDrain), 0x1);
+                __syncwarp();
+                wait_warp(bar(kBarDrain), 0u, abort_flag, kDrainLimitNs, false);
+            }
+        }
+    } else if (warp == kNormWarp) {
+        float *const cn_smem = reinterpret_cast<float *>(sbase + (cn_base - base));
+        const float kNaN = __int_as_float(0x7fc00000);
+        uint32_t n = 0;
+        bool ok = true;
+        for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+            const Unit w = decode_unit<2>(p, u);
+            for (int tile = w.t_begin; tile < w.t_end; ++tile, ++n) {
+                const uint32_t b = n % kCnStages;
+                const uint32_t ph = (n / kCnStages) & 1u;
+                if (!(ok = wait_warp(bar(kBarCnEmpty + b), ph ^ 1u, abort_flag, p.timeout_ns)))
+                    break;
+                const int j = tile * NT;
+#pragma unroll
+                for (int e = 0; e < NT / 32; ++e) {
+                    const int i = e * 32 + lane;
+                    cn_smem[b * NT + i] = (j + i < p.K) ? __ldg(p.cnorm + j + i) : kNaN;
+                }
+                mbar_arrive(bar(kBarCnFull + b));
+            }
+        }
+    } else {
+        // Consumer warp w: TMEM lanes 32*(w%4) .. +31 of this CTA's 128 rows,
+        // columns [col0, col0 + kCW) of every 256-column tile.
+        const int q = warp & 3;
+        const int h = warp >> 2;
+        const int col0 = h * kCW;
+        const uint32_t cn_col = cn_base + 4u * static_cast<uint32_t>(col0);
+        const uint32_t slot = snap_base + 4096u * warp + 16u * lane;
+        const float kNaN = __int_as_float(0x7fc00000);
+        uint32_t acc_used = 0;
+        bool ok = true;
+        for (int u = cluster; u < p.num_units; u += nclusters) {
+            const Unit w = decode_unit<2>(p, u);
+            float best = __int_as_float(0x7f800000);
+            int bi = kNone;
+            for (int tile = w.t_begin; tile < w.t_end; ++tile, ++acc_used) {
+                const uint32_t as = acc_used & 1u;
+                const uint32_t aph = (acc_used >> 1) & 1u;
+                const uint32_t nb = acc_used % kCnStages;
+                const uint32_t nph = (acc_used / kCnStages) & 1u;
+                if (ok)
+                    ok = wait_warp(bar(kBarAccFull + as), aph, abort_flag, p.timeout_ns);
+                if (ok)
+                    ok = wait_warp(bar(kBarCnFull + nb), nph, abort_flag, p.timeout_ns);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t taddr =
+                        tmem_base + (static_cast<uint32_t>(q * 32) << 16) + as * kAccCols + col0;
+                    const uint32_t cn_tile = cn_col + 4u * NT * nb;
+#pragma unroll
+                    for (int g = 0; g < kGroups; ++g) {
+                        __syncwarp();
+                        float v[kGroup][32];
+#pragma unroll
+                        for (int c = 0; c < kGroup; ++c)
+                            tmem_ld_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c]);
+                        tmem_wait_ld();
+                        if (g == kGroups - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if (leader)
+                                    mbar_arrive(bar(kBarAccEmpty + as));
+                                else
+                                    mbar_arrive_cluster(lead_bar(kBarAccEmpty + as));
+                            }
+                        }
+                        float m[kGroup];
+#pragma unroll
+                        for (int c = 0; c < kGroup; ++c) {
+                            apply_norms(v[c], cn_tile + 128u * (g * kGroup + c));
+                            m[c] = chunk_min(v[c]);
+                        }
+                        const int jg = tile * NT + col0 + g * kGroup * 32;
+#pragma unroll
+                        for (int c = 0; c < kGroup; ++c)
+                            fold_chunk<kSnap>(v[c], m[c], jg + 32 * c, best, bi, slot);
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(bar(kBarCnEmpty + nb));
+                }
+            }
+            if (kSnap)
+                resolve_snapshot(best, bi, slot);
+            const int lrow = q * 32 + lane;
+            if (CH > 1) {
+                float *red_s = reinterpret_cast<float *>(sbase + (red_base - base));
+                int *red_i = reinterpret_cast<int *>(red_s + (CH - 1) * kTileM);
+                if (h > 0) {
+                    red_s[(h - 1) * kTileM + lrow] = best;
+                    red_i[(h - 1) * kTileM + lrow] = bi;
+                }
+                named_bar_sync(kConsumerBarrier, 32 * kConsumerWarps);
+                if (h == 0) {
+#pragma unroll
+                    for (int o = 0; o < CH - 1; ++o) {
+                        const float b2 = red_s[o * kTileM + lrow];
+                        const int i2 = red_i[o * kTileM + lrow];
+                        if (b2 < best || (b2 == best && i2 < bi)) {
+                            best = b2;
+                            bi = i2;
+                        }
+                    }
+                }
+            }
+            const int row = w.row0 + static_cast<int>(rank) * kTileM + lrow;
+            if (ok && h == 0 && static_cast<int>(rank) < w.nsub && row < p.N) {
+                if (!w.split) {
+                    float ms;
+                    int ix;
+                    if (bi == kNone) {
+                        ix = 0;
+                        ms = kNaN;
+                    } else {
+                        ix = bi;
+                        ms = (__float_as_uint(best) == 0x80000000u) ? 0.0f : best;
+                    }
+                    p.idx[row] = ix;
+                    if (p.minscore != nullptr)
+                        p.minscore[row] = ms;
+                } else if (bi != kNone) {
+                    atomicMin(p.keys + (row - p.split_row0 * 2 * kTileM), pack_key(best, bi));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // no CTA leaves while its pair can still touch its memory
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+template <int CH, int KB>
+cudaError_t prepare_pair(size_t smem)
+{
+    return cudaFuncSetAttribute(assign_pair_kernel<CH, KB>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+}
+
+template <int CH, int KB>
+cudaError_t launch_pair(const AssignParams &p, const CUtensorMap &xmap, const CUtensorMap &cmap,
+                        int grid, size_t smem, cudaStream_t stream)
+{
+    assign_pair_kernel<CH, KB><<<grid, 32 * (4 * CH + 4), smem, stream>>>(xmap, cmap, p);
+    return cudaGetLastError();
+}
+
+template <int CH>
+cudaError_t dispatch_pair_kb(bool prepare, int kb, const AssignParams *p, const CUtensorMap *xmap,
+                             const CUtensorMap *cmap, int grid, size_t smem, cudaStream_t stream)
+{
+    switch (kb) {
+    case 1:
+        return prepare ? prepare_pair<CH, 1>(smem)
+                       : launch_pair<CH, 1>(*p, *xmap, *cmap, grid, smem, stream);
+    case 2:
+        return prepare ? prepare_pair<CH, 2>(smem)
+                       : launch_pair<CH, 2>(*p, *xmap, *cmap, grid, smem, stream);
+    case 3:
+        return prepare ? prepare_pair<CH, 3>(smem)
+                       : launch_pair<CH, 3>(*p, *xmap, *cmap, grid, smem, stream);
+    case 4:
+        return prepare ? prepare_pair<CH, 4>(smem)
+                       : launch_pair<CH, 4>(*p, *xmap, *cmap, grid, smem, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
 template <int SUB, int NT, int CH, int KB>
 cudaError_t prepare_one(size_t smem)
 {
@@ -662,6 +1068,13 @@ cudaError_t dispatch(bool prepare, const Variant &v, int kb, const AssignParams 
                      const CUtensorMap *xmap, const CUtensorMap *cmap, int grid, size_t smem,
                      cudaStream_t stream)
 {
+    if (v.pair) {
+        if (v.ch == 2)
+            return dispatch_pair_kb<2>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+        if (v.ch == 4)
+            return dispatch_pair_kb<4>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+        return cudaErrorInvalidValue;
+    }
     if (v.sub == 1 && v.nt == 128 && v.ch == 1)
         return dispatch_kb<1, 128, 1>(prepare, kb, p, xmap, cmap, grid, smem, stream);
     if (v.sub == 1 && v.nt == 256 && v.ch == 2)
@@ -677,13 +1090,16 @@ cudaError_t dispatch(bool prepare, const Variant &v, int kb, const AssignParams 
 
 }  // namespace
 
-const Variant kVariants[kNumVariants] = {{2, 128, 1}, {1, 256, 2}, {1, 128, 1}, {2, 128, 2},
-                                         {1, 256, 4}};
+const Variant kVariants[kNumVariants] = {{2, 128, 1, false}, {1, 256, 2, false},
+                                         {1, 128, 1, false}, {2, 128, 2, false},
+                                         {1, 256, 4, false}, {1, 256, 2, true},
+                                         {1, 256, 4, true}};
 
 size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 {
+    const size_t stage_rows = v.pair ? v.nt / 2 : v.nt;
     return 1024 + static_cast<size_t>(xbufs) * v.sub * kblocks * kXTileBytes +
-           static_cast<size_t>(stages) * v.nt * 128 + kCnStages * v.nt * 4 +
+           static_cast<size_t>(stages) * stage_rows * 128 + kCnStages * v.nt * 4 +
            static_cast<size_t>(v.ch - 1) * v.sub * kTileM * 8 +
            (kblocks <= 2 ? static_cast<size_t>(4 * v.sub * v.ch) * 4096 : 0) + kMiscBytes;
 }
@@ -698,6 +1114,32 @@ cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
                           cudaStream_t stream)
 {
     return dispatch(false, v, kblocks, &p, &xmap, &cmap, grid, smem, stream);
+}
+
+cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int *clusters)
+{
+    const void *fn = nullptr;
+    if (v.ch == 2) {
+        const void *t[4] = {(const void *)assign_pair_kernel<2, 1>, (const void *)assign_pair_kernel<2, 2>,
+                            (const void *)assign_pair_kernel<2, 3>, (const void *)assign_pair_kernel<2, 4>};
+        fn = t[kblocks - 1];
+    } else {
+        const void *t[4] = {(const void *)assign_pair_kernel<4, 1>, (const void *)assign_pair_kernel<4, 2>,
+                            (const void *)assign_pair_kernel<4, 3>, (const void *)assign_pair_kernel<4, 4>};
+        fn = t[kblocks - 1];
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(32 * (4 * v.ch + 4), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
 }
 
 cudaError_t status_read_and_clear(int *code)

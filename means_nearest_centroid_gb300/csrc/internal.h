@@ -38,15 +38,19 @@ struct AssignParams {
 
 // Compiled shapes of the assignment kernel: `sub` 128-point sub-tiles per
 // block, `nt` centroids per tensor-core tile, each tile's columns split over
-// `ch` groups of consumer warps.
+// `ch` groups of consumer warps; `pair` kernels tile 256 points per cluster of
+// two blocks.
 struct Variant {
     int sub, nt, ch;
+    bool pair;   // cluster of two CTAs issuing cta_group::2 MMAs (sub 1 per CTA, nt 256)
 };
-constexpr int kNumVariants = 5;
+constexpr int kNumVariants = 7;
 extern const Variant kVariants[kNumVariants];
 
 size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs);
 cudaError_t assign_prepare(const Variant &v, int kblocks, size_t smem_bytes);
+// Clusters of the pair kernel that can be resident at once.
+cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int *clusters);
 cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
                           const CUtensorMap &xmap, const CUtensorMap &cmap, int grid,
                           size_t smem_bytes, cudaStream_t stream);

@@ -28,7 +28,8 @@ def dev():
 
 
 @pytest.mark.parametrize("plan", [dict(), dict(ksplit=3, rows_per_cta=256, centroids_per_tile=128),
-                                  dict(rows_per_cta=128, centroids_per_tile=256, consumer_warps=16)],
+                                  dict(rows_per_cta=128, centroids_per_tile=256, consumer_warps=16),
+                                  dict(rows_per_cta=256, centroids_per_tile=256, consumer_warps=8)],
                          ids=str)
 def test_short_wait_bound_reports_timeout_and_context_survives(dev, plan):
     X, C = workloads.iid(40000, 3000, 128, seed=21)

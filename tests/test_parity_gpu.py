@@ -25,6 +25,8 @@ PLANS = [
     dict(ksplit=-2, rows_per_cta=256, centroids_per_tile=128),
     dict(rows_per_cta=256, centroids_per_tile=128, consumer_warps=16),
     dict(ksplit=2, rows_per_cta=128, centroids_per_tile=256, consumer_warps=16),
+    dict(rows_per_cta=256, centroids_per_tile=256, consumer_warps=8),        # CTA pair
+    dict(ksplit=3, rows_per_cta=256, centroids_per_tile=256, consumer_warps=16),
 ]
 
 
@@ -233,6 +235,8 @@ TAIL_CASES = [
                            consumer_warps=16)),
     (20000, 700, 64, dict(ksplit=-2, rows_per_cta=128, centroids_per_tile=256,
                           consumer_warps=16)),
+    (40000, 700, 256, dict(ksplit=-2, rows_per_cta=256, centroids_per_tile=256,
+                           consumer_warps=8)),
 ]
 
 
