@@ -661,7 +661,7 @@ const char *kmassign_strerror(int code)
         return "kmassign_noalloc: K exceeds its static norm buffer (cnorm NULL needs K <= 1048576)";
     case KMASSIGN_ERR_ARG:
         return "invalid plan value (ksplit != -1, rows_per_cta 128/256, centroids_per_tile "
-               "128/256, not both 256, consumer_warps 4/8/16 matching the shape)";
+               "128/256, consumer_warps 4/8/16 matching a compiled shape)";
     default:
         return "unknown kmassign status code";
     }

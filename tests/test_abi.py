@@ -95,7 +95,7 @@ def test_plan_value_errors(lib):
     assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, -1, 0, 0, 0, NULL) == S["KMASSIGN_ERR_ARG"]
     assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 64, 0, 0, NULL) == S["KMASSIGN_ERR_ARG"]
     assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 0, 96, 0, NULL) == S["KMASSIGN_ERR_ARG"]
-    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 256, 256, 0, NULL) == S["KMASSIGN_ERR_ARG"]
+    assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 0, 0, 32, NULL) == S["KMASSIGN_ERR_ARG"]
     assert ex(A16, A16B, NULL, 10, 5, 64, A16, NULL, 0, 0, 0, 12, NULL) == S["KMASSIGN_ERR_ARG"]
 
 
