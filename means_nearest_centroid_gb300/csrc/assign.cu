@@ -8,8 +8,7 @@
 //
 // Roles inside one thread block (one block per SM, persistent):
 //   * X warp         - TMA-loads the block's X tile once per work unit (the
-//                      tile stays resident while centroids stream past it)
-//                      and asks L2 to prefetch the next unit's X tile;
+//                      tile stays resident while centroids stream past it);
 //   * producer warp  - streams C k-blocks through a ring of shared-memory
 //                      stages guarded by full/empty mbarriers, straight across
 //                      unit boundaries;
@@ -393,16 +392,6 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
                         tma_load_2d(xdst + (t * KB + kb) * kXTileBytes, &xmap, bar(kBarXFull + xb),
                                     kb * kKBlock, w.row0 + t * kTileM, pol_x);
                 ++x_issued;
-                // The next unit's tile comes from L2 when its buffer frees up.
-                const int un = u + static_cast<int>(gridDim.x);
-                if (un < p.num_units) {
-                    const Unit wn = decode_unit<SUB>(p, un);
-                    if (wn.row0 != w.row0)
-                        for (int t = 0; t < wn.nsub; ++t)
-#pragma unroll
-                            for (int kb = 0; kb < KB; ++kb)
-                                tma_prefetch_l2_2d(&xmap, kb * kKBlock, wn.row0 + t * kTileM);
-                }
             }
             if (!ok) {
                 const uint32_t B = p.xbufs;
@@ -772,15 +761,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                                          pol_x);
                 }
                 ++x_issued;
-                const int un = u + nclusters;
-                if (un < p.num_units) {
-                    const Unit wn = decode_unit<2>(p, un);
-                    if (wn.row0 != w.row0 && static_cast<int>(rank) < wn.nsub)
-#pragma unroll
-                        for (int kb = 0; kb < KB; ++kb)
-                            tma_prefetch_l2_2d(&xmap, kb * kKBlock,
-                                               wn.row0 + static_cast<int>(rank) * kTileM);
-                }
             }
             if (!ok) {
                 const uint64_t t0 = globaltimer_ns();
