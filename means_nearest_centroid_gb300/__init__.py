@@ -252,34 +252,71 @@ def assign(X, C, cnorm=None, with_minscore: bool = False, stream=None):
     return (idx, ms) if with_minscore else idx
 
 
-def assign_host(X_host, C_host, idx_host=None, device=None, stream=None, scratch=None):
-    """End-to-end call on host tensors.
+def assign_host(X_host, C_host, idx_host=None, device=None, stream=None, scratch=None,
+                chunks: int = 4):
+    """End-to-end assignment of host tensors (X and C ideally pinned).
 
-    Copies X and C (ideally pinned) to the device, runs the assignment and
-    copies idx back into ``idx_host`` (pinned int32, allocated if None).
-    ``scratch`` may hold preallocated device tensors {"X", "C", "idx"} to
-    reuse.  Returns ``idx_host`` after synchronising the stream.
+    C is copied and its norms computed first; X is copied in ``chunks`` row
+    slices through two device buffers on a copy stream while the previous
+    slice is assigned on the compute stream, and each slice's idx is copied
+    back on a third stream as soon as it is ready.  Every step of the method still runs in the
+    library's kernels; this only overlaps the host<->device copies with them.
+    ``scratch`` may hold preallocated device tensors {"X", "C", "idx"} (X of
+    at least one chunk's rows, C of C_host's shape, idx of N rows).  Returns
+    ``idx_host`` (pinned int32, allocated if None) after synchronising.
     """
     device = torch.device("cuda") if device is None else torch.device(device)
-    s = torch.cuda.current_stream(device) if stream is None else stream
-    N = X_host.shape[0]
+    compute = torch.cuda.current_stream(device) if stream is None else stream
+    N, D = X_host.shape
     if scratch is None:
         scratch = {}
-    with torch.cuda.stream(s):
-        Xd = scratch.get("X")
-        if Xd is None or Xd.shape != X_host.shape:
-            Xd = torch.empty(X_host.shape, dtype=X_host.dtype, device=device)
-        Cd = scratch.get("C")
-        if Cd is None or Cd.shape != C_host.shape:
-            Cd = torch.empty(C_host.shape, dtype=C_host.dtype, device=device)
-        idxd = scratch.get("idx")
-        if idxd is None or idxd.shape[0] != N:
-            idxd = torch.empty(N, dtype=torch.int32, device=device)
-        Xd.copy_(X_host, non_blocking=True)
+    if idx_host is None:
+        idx_host = torch.empty(N, dtype=torch.int32, pin_memory=True)
+    chunks = max(1, min(int(chunks), max(1, N)))
+    rows = (N + chunks - 1) // chunks if N else 0
+    copy = scratch.get("copy_stream")
+    if copy is None:
+        copy = torch.cuda.Stream(device)
+        scratch["copy_stream"] = copy
+    back = scratch.get("back_stream")          # idx copies must not delay X copies
+    if back is None:
+        back = torch.cuda.Stream(device)
+        scratch["back_stream"] = back
+    Cd = scratch.get("C")
+    if Cd is None or Cd.shape != C_host.shape:
+        Cd = torch.empty(C_host.shape, dtype=C_host.dtype, device=device)
+    Xbuf = scratch.get("X")
+    if Xbuf is None or Xbuf.shape[0] < 2 * rows or Xbuf.shape[1] != D:
+        Xbuf = torch.empty((2 * max(rows, 1), D), dtype=X_host.dtype, device=device)
+    idxd = scratch.get("idx")
+    if idxd is None or idxd.shape[0] < N:
+        idxd = torch.empty(max(N, 1), dtype=torch.int32, device=device)
+    cn = torch.empty(C_host.shape[0], dtype=torch.float32, device=device)
+    with torch.cuda.stream(compute):
         Cd.copy_(C_host, non_blocking=True)
-        kmassign(Xd, Cd, idx=idxd, stream=s)
-        if idx_host is None:
-            idx_host = torch.empty(N, dtype=torch.int32, pin_memory=True)
-        idx_host.copy_(idxd, non_blocking=True)
-    s.synchronize()
+        kmassign_norms(Cd, out=cn, stream=compute)
+    done = [None, None]          # compute finished with buffer slot b
+    for c in range(chunks):
+        b0, b1 = c * rows, min(N, (c + 1) * rows)
+        if b0 >= b1:
+            break
+        slot = c % 2
+        xs = Xbuf[slot * rows:slot * rows + (b1 - b0)]
+        with torch.cuda.stream(copy):
+            if done[slot] is not None:
+                copy.wait_event(done[slot])
+            xs.copy_(X_host[b0:b1], non_blocking=True)
+            landed = torch.cuda.Event()
+            landed.record(copy)
+        compute.wait_event(landed)
+        kmassign(xs, Cd, cnorm=cn, idx=idxd[b0:b1], stream=compute)
+        fin = torch.cuda.Event()
+        fin.record(compute)
+        done[slot] = fin
+        with torch.cuda.stream(back):
+            back.wait_event(fin)
+            idx_host[b0:b1].copy_(idxd[b0:b1], non_blocking=True)
+    back.synchronize()
+    copy.synchronize()
+    compute.synchronize()
     return idx_host
