@@ -65,6 +65,8 @@ def load_library(path: str):
     lib.oracle_scores.argtypes = [vp, vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64,
                                   vp, ctypes.c_int]
     lib.oracle_scores.restype = None
+    lib.oracle_update.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp]
+    lib.oracle_update.restype = None
     return lib
 
 
@@ -162,6 +164,33 @@ class Oracle:
         return out
 
 
+def _update(self, X, idx, K):
+    """fp64 per-centroid sums [K, D] and int64 counts [K] of the points by idx."""
+    X = _bits(X)
+    N, D = X.shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    if idx.shape != (N,):
+        raise ValueError("idx must have one entry per point")
+    sums = np.empty((K, D), dtype=np.float64)
+    counts = np.empty(K, dtype=np.int64)
+    self.lib.oracle_update(_ptr(X), _ptr(idx), N, K, D, _ptr(sums), _ptr(counts))
+    return sums, counts
+
+
+def _centroids(self, X, idx, C_old):
+    """Means of the assigned points (fp64), the old centroid where none are assigned."""
+    C_old = _bits(C_old)
+    K, D = C_old.shape
+    sums, counts = self.update(X, idx, K)
+    old = (C_old.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    means = np.where(counts[:, None] > 0, sums / np.maximum(counts, 1)[:, None], old)
+    return means, counts
+
+
+Oracle.update = _update
+Oracle.centroids = _centroids
+
+
 def default() -> Oracle:
     return Oracle()
 
@@ -176,3 +205,11 @@ def assign(X, C, rows=None, cnorm=None, nthreads: int = 0):
 
 def scores(X, C, ii, jj, cnorm=None, nthreads: int = 0):
     return default().scores(X, C, ii, jj, cnorm=cnorm, nthreads=nthreads)
+
+
+def update(X, idx, K):
+    return default().update(X, idx, K)
+
+
+def centroids(X, idx, C_old):
+    return default().centroids(X, idx, C_old)

@@ -150,3 +150,29 @@ void oracle_scores(const uint16_t *X, const uint16_t *C, const double *cnorm, in
     for (int64_t p = 0; p < npairs; ++p)
         out[p] = score(X + ii[p] * D, C + jj[p] * D, cnorm[jj[p]], D);
 }
+
+/*
+ * The k-means update step, which follows the assignment in a Lloyd iteration
+ * (flashlib PR #22 covers the assignment only; this is the textbook update):
+ * for every centroid j,
+ *   counts[j] = number of points with idx[i] == j
+ *   sums[j][d] = sum over those points, in increasing i, of x_id (fp64)
+ * idx values outside [0, K) are skipped.
+ */
+void oracle_update(const uint16_t *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
+                   double *sums, int64_t *counts)
+{
+    for (int64_t j = 0; j < K; ++j) {
+        counts[j] = 0;
+        for (int64_t d = 0; d < D; ++d)
+            sums[j * D + d] = 0.0;
+    }
+    for (int64_t i = 0; i < N; ++i) {
+        int32_t j = idx[i];
+        if (j < 0 || j >= K)
+            continue;
+        counts[j] += 1;
+        for (int64_t d = 0; d < D; ++d)
+            sums[(int64_t)j * D + d] += bf16_to_double(X[i * D + d]);
+    }
+}

@@ -209,3 +209,82 @@ def check_subsets_consistent(orc):
 
 ALL_CHECKS = [check_golden, check_bruteforce_rational, check_distance_identity,
               check_numpy_argmin, check_single_infinity_rows, check_subsets_consistent]
+
+
+# ---------------------------------------------------------------- update step
+def _exact_update(Xf, idx, K, D):
+    sums = [[Fraction(0)] * D for _ in range(K)]
+    counts = [0] * K
+    for x, j in zip(Xf, idx):
+        if 0 <= j < K:
+            counts[j] += 1
+            for d in range(D):
+                sums[j][d] += x[d]
+    return sums, counts
+
+
+def check_update_rational(orc, trials: int = 12):
+    rng = np.random.default_rng(321)
+    for t in range(trials):
+        N = int(rng.integers(0, 30))
+        K = int(rng.integers(1, 9))
+        D = int(rng.integers(1, 12))
+        X, _ = workloads.iid(N, 1, D, seed=70 + t)
+        idx = rng.integers(-1, K + 1, N).astype(np.int32)     # includes invalid ids
+        sums, counts = orc.update(X, idx, K)
+        exp_s, exp_c = _exact_update(_exact(X), idx.tolist(), K, D)
+        assert list(counts) == exp_c, t
+        for j in range(K):
+            for d in range(D):
+                assert Fraction(float(sums[j, d])) == exp_s[j][d], (t, j, d)
+
+
+def check_update_invariants(orc):
+    X, C = workloads.integers(500, 23, 40, seed=11)
+    idx, _ = orc.assign(X, C)
+    sums, counts = orc.update(X, idx, 23)
+    xs = X.to(torch.float64).numpy()
+    assert counts.sum() == 500
+    assert np.array_equal(sums.sum(0), xs.sum(0))                   # integers: exact
+    perm = np.random.default_rng(3).permutation(500)
+    s2, c2 = orc.update(X[perm], idx[perm], 23)
+    assert np.array_equal(s2, sums) and np.array_equal(c2, counts)   # order-free on integers
+    for j in (0, 5, 22):
+        assert np.array_equal(sums[j], xs[idx == j].sum(0))
+
+
+def check_lloyd_descent(orc):
+    """For a fixed assignment the mean minimises the summed squared distance:
+    replacing each used centroid by its points' mean never raises it."""
+    X, C = workloads.blobs(400, 12, 16, seed=5)
+    idx, _ = orc.assign(X, C)
+    xs = X.to(torch.float64).numpy()
+    cs = C.to(torch.float64).numpy()
+    means, counts = orc.centroids(X, idx, C)
+    before = ((xs - cs[idx]) ** 2).sum()
+    after = ((xs - means[idx]) ** 2).sum()
+    assert after <= before * (1 + 1e-12)
+    # and any perturbation of a mean raises it (first-order optimality)
+    j = int(np.argmax(counts))
+    for delta in (1e-3, -1e-3):
+        m2 = means.copy()
+        m2[j, 0] += delta
+        assert ((xs - m2[idx]) ** 2).sum() > after
+
+
+def check_empty_cluster_keeps_centroid(orc):
+    X, C = workloads.integers(20, 6, 8, seed=4)
+    idx = np.zeros(20, dtype=np.int32)
+    idx[10:] = 3
+    means, counts = orc.centroids(X, idx, C)
+    cs = C.to(torch.float64).numpy()
+    xs = X.to(torch.float64).numpy()
+    assert list(counts) == [10, 0, 0, 10, 0, 0]
+    for j in (1, 2, 4, 5):
+        assert np.array_equal(means[j], cs[j])
+    assert np.array_equal(means[0], xs[:10].mean(0))
+    assert np.array_equal(means[3], xs[10:].mean(0))
+
+
+ALL_CHECKS += [check_update_rational, check_update_invariants, check_lloyd_descent,
+               check_empty_cluster_keeps_centroid]

@@ -32,6 +32,13 @@ MUTANTS = {
     "fp32_dot_accumulator": ("    double acc = 0.0;\n    for (int64_t d = 0; d < D; ++d)\n        acc += bf16",
                              "    float acc = 0.0f;\n    for (int64_t d = 0; d < D; ++d)\n        acc += (float)bf16"),
     "centroid_index_off_by_one": ("score(x, C + j * D, cnorm[j], D)", "score(x, C + j * D, cnorm[j > 0 ? j - 1 : 0], D)"),
+    "update_counts_twice": ("        counts[j] += 1;", "        counts[j] += 2;"),
+    "update_wrong_dimension": ("sums[(int64_t)j * D + d] += bf16_to_double(X[i * D + d]);",
+                               "sums[(int64_t)j * D + d] += bf16_to_double(X[i * D + (d + 1) % D]);"),
+    "update_keeps_invalid_ids": ("        if (j < 0 || j >= K)\n            continue;",
+                                 "        if (j < 0 || j >= K)\n            j = 0;"),
+    "update_skips_first_point": ("    for (int64_t i = 0; i < N; ++i) {\n        int32_t j",
+                                 "    for (int64_t i = 1; i < N; ++i) {\n        int32_t j"),
 }
 
 
