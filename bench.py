@@ -331,6 +331,68 @@ def run_pages_shapes(device):
     return 0
 
 
+def run_update_bench(device, key, steps, warmup):
+    """The update step (kmassign_update) on a workload, against the HBM roofline,
+    and one whole Lloyd iteration (norms + assignment + update + centroids).
+    Three rotating input sets, as in the main benchmark.  One JSON line."""
+    import means_nearest_centroid_gb300 as km
+    w = workloads.WORKLOADS[key]
+    N, D, K = w.N, w.D, w.K
+    stream = torch.cuda.current_stream(device)
+    sets = []
+    for v in range(3):
+        X, C = workloads.make(key, variant=v)
+        Xd, Cd = X.to(device), C.to(device)
+        sets.append((Xd, Cd, km.kmassign(Xd, Cd, stream=stream)))
+    sums = torch.zeros((K, D), dtype=torch.float32, device=device)
+    counts = torch.zeros(K, dtype=torch.int32, device=device)
+    for i in range(warmup):
+        Xd, Cd, idx = sets[i % 3]
+        km.kmassign_update(Xd, idx, K, sums=sums, counts=counts, stream=stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        Xd, Cd, idx = sets[i % 3]
+        sums.zero_()
+        counts.zero_()
+        evs[i][0].record(stream)
+        km.kmassign_update(Xd, idx, K, sums=sums, counts=counts, stream=stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    upd_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    alg_bytes = 2 * N * D + 4 * N + 8 * K * D + 4 * K
+    # a whole iteration on the device
+    Cw = sets[0][1].clone()
+    km.kmassign_lloyd(sets[0][0], Cw, iters=2, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    km.kmassign_lloyd(sets[0][0], Cw, iters=steps, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    it_ms = e0.elapsed_time(e1) / steps
+    rc = km.kmassign_check(stream)
+    line = {"metric": "k-means update step GB/s (algorithmic bytes / t) and Lloyd iteration ms",
+            "value": alg_bytes / (upd_ms * 1e-3) / 1e9, "unit": "GB/s", "steps": steps,
+            "warmup": warmup, "higher_is_better": True, "dtype": "bf16 in, fp32 sums",
+            "data": "synthetic", "status": rc,
+            "config": {"workload": w.text, "key": key, "N": N, "D": D, "K": K},
+            "update_ms": upd_ms,
+            "roofline": {"bound": "hbm", "achieved": alg_bytes / (upd_ms * 1e-3) / 1e9,
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": alg_bytes / (upd_ms * 1e-3) / 1e9 / hbm,
+                         "peak_source": f"{src} copy bandwidth", "traffic": None,
+                         "algorithmic_bytes": alg_bytes},
+            "lloyd_iteration_ms": it_ms,
+            "lloyd_iteration_tflops": 2.0 * N * K * D / (it_ms * 1e-3) / 1e12}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -344,6 +406,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pages-shapes", action="store_true",
                     help="time the pages' 13 benchmark shapes instead (context table)")
+    ap.add_argument("--update", action="store_true",
+                    help="time the update step and a Lloyd iteration instead")
     ap.add_argument("--parity-rows", type=int, default=256)
     ap.add_argument("--N", type=int, default=None, help="override the workload's N")
     ap.add_argument("--K", type=int, default=None, help="override the workload's K")
@@ -360,10 +424,12 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    if args.pages_shapes:
+    if args.pages_shapes or args.update:
         from means_nearest_centroid_gb300 import _build
         _build.build()
-        return run_pages_shapes(device)
+        if args.pages_shapes:
+            return run_pages_shapes(device)
+        return run_update_bench(device, key, args.steps, args.warmup)
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)

@@ -159,6 +159,42 @@ int kmassign_noalloc(const void *X, const void *C, const float *cnorm, int64_t N
                      int64_t D, int32_t *idx, float *minscore, void *stream);
 
 /*
+ * The update step of a Lloyd iteration (the textbook step after the
+ * assignment; flashlib PR #22 covers the assignment only):
+ *     counts[j] += |{i : idx[i] == j}|,   sums[j][d] += sum of x_id over them
+ *   X       device, bf16 [N, D] row-major, 16-byte aligned
+ *   idx     device int32 [N] (ids outside [0, K) are skipped)
+ *   sums    device fp32 [K, D], 16-byte aligned, accumulated into
+ *   counts  device int32 [K], accumulated into
+ * The caller zeroes sums and counts first, or keeps accumulating over batches
+ * (or adds the results of several GPUs).  Sums are fp32 additions in an
+ * unspecified order: on non-integer data their last bits can differ from run
+ * to run; integer-valued data whose sums stay below 2^24 is exact.
+ */
+int kmassign_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
+                    float *sums, int32_t *counts, void *stream);
+
+/*
+ * New centroids from kmassign_update's results: C_new[j] = bf16(sums[j] /
+ * counts[j]) (fp32 division, then round to nearest even) where counts[j] > 0,
+ * else C_old[j].  means (fp32 [K, D], 16-byte aligned) receives the unrounded
+ * means when not NULL.  C_new may be C_old.  All pointers device memory.
+ */
+int kmassign_centroids(const float *sums, const int32_t *counts, const void *C_old, int64_t K,
+                       int64_t D, void *C_new, float *means, void *stream);
+
+/*
+ * `iters` Lloyd iterations on the device: each assigns X to C (norms computed
+ * inside) into idx, then replaces every centroid that received points by
+ * their mean (kmassign_update + kmassign_centroids), in place in C.  On
+ * return idx holds the last assignment, made with the centroids before the
+ * last update.  Temporaries (sums, counts, norms) come from the library's
+ * stream-ordered pool.  iters < 0 returns KMASSIGN_ERR_ARG.
+ */
+int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int iters,
+                   int32_t *idx, void *stream);
+
+/*
  * Bound, in nanoseconds of the GPU's global timer, on every pipeline wait in
  * the kernels launched afterwards by this process (0 restores the default,
  * 2 s).  A wait that runs out aborts its kernel cleanly and makes

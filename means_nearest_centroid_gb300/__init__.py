@@ -23,7 +23,8 @@ from . import _build
 
 __all__ = [
     "KmassignError", "library", "library_path", "kmassign", "kmassign_ex", "kmassign_norms",
-    "kmassign_noalloc", "kmassign_set_wait_timeout", "shard_rows",
+    "kmassign_noalloc", "kmassign_set_wait_timeout", "shard_rows", "kmassign_update",
+    "kmassign_centroids", "kmassign_lloyd",
     "kmassign_plan", "kmassign_check", "kmassign_strerror", "assign", "norms", "assign_host",
     "STATUS",
 ]
@@ -68,6 +69,12 @@ def _declare(lib):
     lib.kmassign_noalloc.restype = i32
     lib.kmassign_plan.argtypes = [i64, i64, i64, vp]
     lib.kmassign_plan.restype = i32
+    lib.kmassign_update.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
+    lib.kmassign_update.restype = i32
+    lib.kmassign_centroids.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp]
+    lib.kmassign_centroids.restype = i32
+    lib.kmassign_lloyd.argtypes = [vp, vp, i64, i64, i64, i32, vp, vp]
+    lib.kmassign_lloyd.restype = i32
     lib.kmassign_set_wait_timeout.argtypes = [ctypes.c_uint64]
     lib.kmassign_set_wait_timeout.restype = i32
     lib.kmassign_check.argtypes = [vp]
@@ -214,6 +221,61 @@ def kmassign_plan(N: int, K: int, D: int) -> dict:
     keys = ["ksplit", "rows_per_cta", "centroids_per_tile", "grid", "stages", "xbufs",
             "whole_row_tiles", "split_row_tiles", "consumer_warps"]
     return dict(zip(keys, list(out)))
+
+
+def kmassign_update(X, idx, K: int, sums=None, counts=None, stream=None):
+    """Per-centroid fp32 sums [K, D] and int32 counts [K] of X's rows by idx.
+
+    When sums/counts are given they are accumulated into; otherwise zeroed
+    tensors are created.  Returns (sums, counts).
+    """
+    _need_cuda(X, "X", torch.bfloat16)
+    _need_cuda(idx, "idx", torch.int32)
+    N, D = X.shape
+    if idx.shape != (N,):
+        raise ValueError("idx must hold one id per point")
+    if sums is None:
+        sums = torch.zeros((K, D), dtype=torch.float32, device=X.device)
+    if counts is None:
+        counts = torch.zeros(K, dtype=torch.int32, device=X.device)
+    _need_cuda(sums, "sums", torch.float32)
+    _need_cuda(counts, "counts", torch.int32)
+    _check(library().kmassign_update(_ptr(X), _ptr(idx), N, int(K), D, _ptr(sums), _ptr(counts),
+                                     _stream_ptr(stream)), "kmassign_update")
+    return sums, counts
+
+
+def kmassign_centroids(sums, counts, C_old, C_new=None, means=None, stream=None):
+    """bf16 means of the assigned points (C_old where a centroid has none)."""
+    _need_cuda(sums, "sums", torch.float32)
+    _need_cuda(counts, "counts", torch.int32)
+    _need_cuda(C_old, "C_old", torch.bfloat16)
+    K, D = C_old.shape
+    if C_new is None:
+        C_new = torch.empty_like(C_old)
+    _need_cuda(C_new, "C_new", torch.bfloat16)
+    if means is not None:
+        _need_cuda(means, "means", torch.float32)
+    _check(library().kmassign_centroids(_ptr(sums), _ptr(counts), _ptr(C_old), K, D, _ptr(C_new),
+                                        _ptr(means), _stream_ptr(stream)), "kmassign_centroids")
+    return C_new
+
+
+def kmassign_lloyd(X, C, iters: int, idx=None, stream=None):
+    """``iters`` Lloyd iterations on the GPU, updating C (bf16) in place.
+
+    Returns idx, the last assignment (made before the last update).
+    """
+    _need_cuda(X, "X", torch.bfloat16)
+    _need_cuda(C, "C", torch.bfloat16)
+    N, D = X.shape
+    K = C.shape[0]
+    if idx is None:
+        idx = torch.empty(N, dtype=torch.int32, device=X.device)
+    _need_cuda(idx, "idx", torch.int32)
+    _check(library().kmassign_lloyd(_ptr(X), _ptr(C), N, K, D, int(iters), _ptr(idx),
+                                    _stream_ptr(stream)), "kmassign_lloyd")
+    return idx
 
 
 def kmassign_set_wait_timeout(ns: int) -> None:

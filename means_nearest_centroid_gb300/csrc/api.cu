@@ -447,6 +447,133 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
 }  // namespace
 
 // ---------------------------------------------------------------------------
+// The update step and the Lloyd loop.
+
+namespace {
+
+int check_update_args(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
+                      const float *sums, const int32_t *counts)
+{
+    int rc = check_shape(N, K, D);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    if (N > 0 && (X == nullptr || idx == nullptr))
+        return KMASSIGN_ERR_NULL;
+    if (sums == nullptr || counts == nullptr)
+        return KMASSIGN_ERR_NULL;
+    if ((X && !aligned(X, 16)) || (idx && !aligned(idx, 4)) || !aligned(sums, 16) ||
+        !aligned(counts, 4))
+        return KMASSIGN_ERR_ALIGN;
+    return KMASSIGN_OK;
+}
+
+int run_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D, float *sums,
+               int32_t *counts, cudaStream_t stream)
+{
+    int rc = check_update_args(X, idx, N, K, D, sums, counts);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    if (N == 0)
+        return KMASSIGN_OK;
+    const void *ptrs[4] = {X, idx, sums, counts};
+    if ((rc = check_device_ptrs(ptrs, 4)) != KMASSIGN_OK)
+        return rc;
+    DeviceInfo dev;
+    if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
+        return rc;
+    if (kma::launch_update(X, idx, N, K, D, sums, counts, dev.sms, stream) != cudaSuccess)
+        return KMASSIGN_ERR_CUDA;
+    return KMASSIGN_OK;
+}
+
+int run_centroids(const float *sums, const int32_t *counts, const void *C_old, int64_t K,
+                  int64_t D, void *C_new, float *means, cudaStream_t stream)
+{
+    int rc = check_shape(0, K, D);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    if (sums == nullptr || counts == nullptr || C_old == nullptr || C_new == nullptr)
+        return KMASSIGN_ERR_NULL;
+    if (!aligned(sums, 16) || !aligned(counts, 4) || !aligned(C_old, 16) || !aligned(C_new, 16) ||
+        (means && !aligned(means, 16)))
+        return KMASSIGN_ERR_ALIGN;
+    const void *ptrs[5] = {sums, counts, C_old, C_new, means};
+    if ((rc = check_device_ptrs(ptrs, 5)) != KMASSIGN_OK)
+        return rc;
+    if (kma::launch_centroids(sums, counts, C_old, K, D, C_new, means, stream) != cudaSuccess)
+        return KMASSIGN_ERR_CUDA;
+    return KMASSIGN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kmassign_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
+                    float *sums, int32_t *counts, void *stream)
+{
+    return run_update(X, idx, N, K, D, sums, counts, static_cast<cudaStream_t>(stream));
+}
+
+int kmassign_centroids(const float *sums, const int32_t *counts, const void *C_old, int64_t K,
+                       int64_t D, void *C_new, float *means, void *stream)
+{
+    return run_centroids(sums, counts, C_old, K, D, C_new, means,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int iters,
+                   int32_t *idx, void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = check_shape(N, K, D);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    if (iters < 0)
+        return KMASSIGN_ERR_ARG;
+    if (N == 0 || iters == 0)
+        return KMASSIGN_OK;
+    if (X == nullptr || C == nullptr || idx == nullptr)
+        return KMASSIGN_ERR_NULL;
+    if (!aligned(X, 16) || !aligned(C, 16) || !aligned(idx, 4))
+        return KMASSIGN_ERR_ALIGN;
+    const void *ptrs[3] = {X, C, idx};
+    if ((rc = check_device_ptrs(ptrs, 3)) != KMASSIGN_OK)
+        return rc;
+    DeviceInfo dev;
+    if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
+        return rc;
+    float *sums = nullptr;
+    int32_t *counts = nullptr;
+    const size_t sum_bytes = static_cast<size_t>(K) * D * 4;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&sums), sum_bytes, dev.pool, s) !=
+            cudaSuccess ||
+        cudaMallocFromPoolAsync(reinterpret_cast<void **>(&counts), static_cast<size_t>(K) * 4,
+                                dev.pool, s) != cudaSuccess) {
+        if (sums != nullptr)
+            cudaFreeAsync(sums, s);
+        return KMASSIGN_ERR_CUDA;
+    }
+    for (int it = 0; rc == KMASSIGN_OK && it < iters; ++it) {
+        // assignment with the current centroids (norms computed inside) ...
+        rc = run_assign(X, C, nullptr, N, K, D, idx, nullptr, 0, 0, 0, 0, s);
+        if (rc != KMASSIGN_OK)
+            break;
+        // ... then the means of the assigned points replace them in place
+        if (cudaMemsetAsync(sums, 0, sum_bytes, s) != cudaSuccess ||
+            cudaMemsetAsync(counts, 0, static_cast<size_t>(K) * 4, s) != cudaSuccess ||
+            kma::launch_update(X, idx, N, K, D, sums, counts, dev.sms, s) != cudaSuccess ||
+            kma::launch_centroids(sums, counts, C, K, D, C, nullptr, s) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+    }
+    if (cudaFreeAsync(sums, s) != cudaSuccess || cudaFreeAsync(counts, s) != cudaSuccess)
+        rc = KMASSIGN_ERR_CUDA;
+    return rc;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
 // kmassign_noalloc: the assignment call for callers that must not allocate.
 //
 // Some callers cannot have a library allocate device memory behind their

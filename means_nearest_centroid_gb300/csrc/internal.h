@@ -56,6 +56,10 @@ cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
                           size_t smem_bytes, cudaStream_t stream);
 
 cudaError_t launch_norms(const void *C, int64_t K, int64_t D, float *cnorm, cudaStream_t stream);
+cudaError_t launch_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
+                          float *sums, int32_t *counts, int sms, cudaStream_t stream);
+cudaError_t launch_centroids(const float *sums, const int32_t *counts, const void *C_old, int64_t K,
+                             int64_t D, void *C_new, float *means, cudaStream_t stream);
 cudaError_t launch_finalize(const unsigned long long *keys, int64_t N, int32_t *idx,
                             float *minscore, cudaStream_t stream);
 

@@ -1,0 +1,136 @@
+"""The update step and the Lloyd loop on the GPU vs the fp64 oracle (GB300).
+
+Rules: counts are integers and must match exactly.  Sums are fp32 additions
+in an unspecified order; for centroid j and dimension d the bound is
+    |gpu - exact| <= n_j * 2^-24 * sum_i |x_id|        (order-free fp32 bound)
+plus exact equality on integer-valued data (every partial sum is an integer
+below 2^24).  Means are sums / counts with one more rounding.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import means_nearest_centroid_gb300 as km
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+U = 2.0 ** -24
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from means_nearest_centroid_gb300 import _build
+    _build.build()
+    km.library()
+    return torch.device("cuda:0")
+
+
+def _abs_sums(X, idx, K):
+    xs = np.abs(X.to(torch.float64).numpy())
+    out = np.zeros((K, X.shape[1]))
+    ok = (idx >= 0) & (idx < K)
+    np.add.at(out, idx[ok], xs[ok])
+    return out
+
+
+def check_sums(X, idx, K, sums, counts, integer):
+    o_sums, o_counts = oracle.update(X, idx, K)
+    assert np.array_equal(counts.cpu().numpy().astype(np.int64), o_counts)
+    g = sums.cpu().double().numpy()
+    if integer:
+        assert np.array_equal(g, o_sums)
+    else:
+        bound = o_counts[:, None] * U * _abs_sums(X, idx, K) + 1e-30
+        assert np.all(np.abs(g - o_sums) <= bound), float(np.max(np.abs(g - o_sums) - bound))
+
+
+@pytest.mark.parametrize("N,K,D", [(1, 1, 16), (1000, 37, 64), (5000, 300, 128), (3000, 17, 256),
+                                   (2048, 1000, 48), (999, 5, 80)])
+def test_update_float_and_integer(dev, N, K, D):
+    X, C = workloads.blobs(N, K, D, seed=N + D)
+    g = np.random.default_rng(N)
+    idx = g.integers(-2, K + 2, N).astype(np.int32)          # includes ids to skip
+    sums, counts = km.kmassign_update(X.to(dev), torch.from_numpy(idx).to(dev), K)
+    check_sums(X, idx, K, sums, counts, integer=False)
+    Xi, _ = workloads.integers(N, K, D, seed=N * 3)
+    sums, counts = km.kmassign_update(Xi.to(dev), torch.from_numpy(idx).to(dev), K)
+    check_sums(Xi, idx, K, sums, counts, integer=True)
+
+
+def test_update_accumulates_batches(dev):
+    X, _ = workloads.integers(4000, 1, 64, seed=8)
+    idx = np.random.default_rng(1).integers(0, 50, 4000).astype(np.int32)
+    Xd, idxd = X.to(dev), torch.from_numpy(idx).to(dev)
+    sums, counts = km.kmassign_update(Xd[:1500], idxd[:1500], 50)
+    km.kmassign_update(Xd[1500:], idxd[1500:], 50, sums=sums, counts=counts)
+    check_sums(X, idx, 50, sums, counts, integer=True)
+
+
+def test_centroids_means_rounding_and_empty(dev):
+    X, C = workloads.blobs(3000, 64, 128, seed=2)
+    idx = np.random.default_rng(2).integers(0, 60, 3000).astype(np.int32)   # 60..63 empty
+    Xd, Cd = X.to(dev), C.to(dev)
+    sums, counts = km.kmassign_update(Xd, torch.from_numpy(idx).to(dev), 64)
+    means = torch.empty(64, 128, dtype=torch.float32, device=dev)
+    Cn = km.kmassign_centroids(sums, counts, Cd, means=means)
+    o_means, o_counts = oracle.centroids(X, idx, C)
+    m = means.cpu().double().numpy()
+    bound = (o_counts[:, None] * U * _abs_sums(X, idx, 64) / np.maximum(o_counts, 1)[:, None]
+             + np.abs(o_means) * U + 1e-30)
+    assert np.all(np.abs(m - o_means) <= bound)
+    # bf16 output is the round-to-nearest-even of the fp32 means
+    assert torch.equal(Cn.cpu().view(torch.int16), means.cpu().to(torch.bfloat16).view(torch.int16))
+    # empty clusters keep their centroid bit for bit
+    assert torch.equal(Cn[60:].cpu().view(torch.int16), C[60:].view(torch.int16))
+    # in place
+    Cd2 = Cd.clone()
+    km.kmassign_centroids(sums, counts, Cd2, C_new=Cd2)
+    assert torch.equal(Cd2, Cn)
+
+
+def test_lloyd_matches_host_driven_pieces(dev):
+    X, C0 = workloads.adversarial(6000, 512, 64, seed=6)
+    Xd = X.to(dev)
+    C_loop = C0.to(dev).clone()
+    idx_loop = km.kmassign_lloyd(Xd, C_loop, iters=3)
+    assert km.kmassign_check() == 0
+    C = C0.to(dev).clone()
+    for _ in range(3):
+        idx = km.kmassign(Xd, C)
+        sums, counts = km.kmassign_update(Xd, idx, 512)
+        km.kmassign_centroids(sums, counts, C, C_new=C)
+    assert torch.equal(idx_loop, idx)
+    assert torch.equal(C_loop.view(torch.int16), C.view(torch.int16))
+
+
+def test_lloyd_one_iteration_vs_oracle(dev):
+    X, C0 = workloads.integers(3000, 40, 32, seed=12)
+    Xd = X.to(dev)
+    C = C0.to(dev).clone()
+    idx = km.kmassign_lloyd(Xd, C, iters=1)
+    o_idx, _ = oracle.assign(X, C0)
+    assert np.array_equal(idx.cpu().numpy(), o_idx)
+    o_means, o_counts = oracle.centroids(X, o_idx, C0)
+    # integer sums are exact; the GPU divides in fp32 then rounds to bf16, so
+    # its centroid is within one bf16 step of the exact mean
+    got = C.cpu().double().numpy()
+    assert np.all(np.abs(got - o_means) <= np.abs(o_means) * 2.0 ** -8 + 1e-30)
+
+
+def test_lloyd_rejects_negative_iterations(dev):
+    X, C = workloads.integers(10, 4, 16, seed=1)
+    with pytest.raises(km.KmassignError):
+        km.kmassign_lloyd(X.to(dev), C.to(dev), iters=-1)
+
+
+def test_update_full_size_lognormal(dev):
+    w = workloads.WORKLOADS["lognormal_clusters"]
+    X, C = workloads.make("lognormal_clusters")
+    Xd, Cd = X.to(dev), C.to(dev)
+    idx = km.kmassign(Xd, Cd)
+    sums, counts = km.kmassign_update(Xd, idx, w.K)
+    check_sums(X, idx.cpu().numpy(), w.K, sums, counts, integer=False)
