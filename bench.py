@@ -116,7 +116,7 @@ def kernel_source_sha() -> str:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -136,7 +136,7 @@ class ClockSampler:
         except Exception:
             target = None
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "50"]
+               "-lms", "20"]
         if target:
             cmd += ["-i", target]
         try:
@@ -396,7 +396,7 @@ def run_update_bench(device, key, steps, warmup):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="iid_normal", choices=list(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -193,6 +193,15 @@ def test_non_default_stream(dev):
     assert rep.ok(), rep
 
 
+def test_many_centroids(dev):
+    """K = 100,000 (many tiles, a ragged last tile, plans that split K)."""
+    X, C = workloads.blobs(3000, 100000, 16, seed=77)
+    idx, ms = run(dev, X, C)
+    rows = np.arange(0, 3000, 7)
+    rep = parity.compare(X, C, idx, ms, rows=rows)
+    assert rep.ok(), rep
+
+
 # ---------------------------------------------------------------- full sizes
 FULL_SAMPLE = {"tiny_blobs": None, "sampled_centroids": 8192, "iid_normal": 2048,
                "lognormal_clusters": 4096, "adversarial_ties": None}
