@@ -67,6 +67,9 @@ def load_library(path: str):
     lib.oracle_scores.restype = None
     lib.oracle_update.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp]
     lib.oracle_update.restype = None
+    lib.oracle_topk.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp,
+                                ctypes.c_int64, ctypes.c_int64, vp, vp, ctypes.c_int]
+    lib.oracle_topk.restype = None
     return lib
 
 
@@ -187,6 +190,29 @@ def _centroids(self, X, idx, C_old):
     return means, counts
 
 
+def _topk(self, X, C, k, rows=None, cnorm=None, nthreads: int = 0):
+    """(idx int32 [rows, k], score float64 [rows, k]): the k nearest centroids."""
+    X = _bits(X)
+    C = _bits(C)
+    N, D = X.shape
+    K = C.shape[0]
+    if not 1 <= k <= K:
+        raise ValueError("need 1 <= k <= K")
+    if cnorm is None:
+        cnorm = self.norms(C, nthreads)
+    cnorm = np.ascontiguousarray(cnorm, dtype=np.float64)
+    rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nrows = N if rows_arr is None else rows_arr.size
+    idx = np.empty((nrows, k), dtype=np.int32)
+    sc = np.empty((nrows, k), dtype=np.float64)
+    if nrows:
+        self.lib.oracle_topk(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D,
+                             None if rows_arr is None else _ptr(rows_arr), nrows, k, _ptr(idx),
+                             _ptr(sc), int(nthreads))
+    return idx, sc
+
+
+Oracle.topk = _topk
 Oracle.update = _update
 Oracle.centroids = _centroids
 
@@ -209,6 +235,10 @@ def scores(X, C, ii, jj, cnorm=None, nthreads: int = 0):
 
 def update(X, idx, K):
     return default().update(X, idx, K)
+
+
+def topk(X, C, k, rows=None, cnorm=None, nthreads: int = 0):
+    return default().topk(X, C, k, rows=rows, cnorm=cnorm, nthreads=nthreads)
 
 
 def centroids(X, idx, C_old):

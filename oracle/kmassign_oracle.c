@@ -176,3 +176,53 @@ void oracle_update(const uint16_t *X, const int32_t *idx, int64_t N, int64_t K, 
             sums[(int64_t)j * D + d] += bf16_to_double(X[i * D + d]);
     }
 }
+
+/*
+ * The k nearest centroids of each point: the k smallest pairs (s_ij, j) in
+ * the order the assignment uses (NaN above every number, -0 equal to +0, the
+ * lower index first among equal scores), ascending.  With k = 1 this is the
+ * assignment itself.  Requires 1 <= k <= K.  rows as in oracle_assign;
+ * results go to idx[r * k + e] and score[r * k + e].
+ */
+static int pair_less(double a, int64_t ja, double b, int64_t jb)
+{
+    if (score_less(a, b))
+        return 1;
+    if (score_less(b, a))
+        return 0;
+    return ja < jb;   /* equal scores, or both NaN */
+}
+
+void oracle_topk(const uint16_t *X, const uint16_t *C, const double *cnorm, int64_t N, int64_t K,
+                 int64_t D, const int64_t *rows, int64_t nrows, int64_t k, int32_t *idx,
+                 double *score_out, int nthreads)
+{
+    (void)N;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        const uint16_t *xi = X + i * D;
+        int32_t *bi = idx + r * k;
+        double *bs = score_out + r * k;
+        int64_t filled = 0;
+        for (int64_t j = 0; j < K; ++j) {
+            double s = score(xi, C + j * D, cnorm[j], D);
+            /* insert (s, j) into the sorted list bs/bi of length filled (<= k) */
+            int64_t pos = filled;
+            while (pos > 0 && pair_less(s, j, bs[pos - 1], bi[pos - 1]))
+                --pos;
+            if (pos >= k)
+                continue;
+            int64_t last = filled < k ? filled : k - 1;
+            for (int64_t e = last; e > pos; --e) {
+                bs[e] = bs[e - 1];
+                bi[e] = bi[e - 1];
+            }
+            bs[pos] = s;
+            bi[pos] = (int32_t)j;
+            if (filled < k)
+                ++filled;
+        }
+    }
+}

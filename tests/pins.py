@@ -288,3 +288,48 @@ def check_empty_cluster_keeps_centroid(orc):
 
 ALL_CHECKS += [check_update_rational, check_update_invariants, check_lloyd_descent,
                check_empty_cluster_keeps_centroid]
+
+
+# ---------------------------------------------------------------- top-k
+def check_topk_rational(orc, trials: int = 12):
+    rng = np.random.default_rng(99)
+    for t in range(trials):
+        N = int(rng.integers(1, 7))
+        K = int(rng.integers(1, 14))
+        D = int(rng.integers(1, 10))
+        k = int(rng.integers(1, K + 1))
+        X, C = (workloads.integers(N, K, D, seed=40 + t, lo=-2, hi=2) if t % 2 == 0
+                else workloads.iid(N, K, D, seed=40 + t))
+        Xf, Cf = _exact(X), _exact(C)
+        norms = [sum(c * c for c in row) for row in Cf]
+        idx, sc = orc.topk(X, C, k)
+        for r, x in enumerate(Xf):
+            s = [(norms[j] - 2 * sum(a * b for a, b in zip(x, Cf[j])), j) for j in range(K)]
+            s.sort()                                   # exact: by score, then index
+            assert [j for _, j in s[:k]] == list(idx[r]), (t, r)
+            for e in range(k):
+                assert abs(Fraction(float(sc[r, e])) - s[e][0]) <= Fraction(1, 2**40) * (1 + abs(s[e][0]))
+
+
+def check_topk_consistency(orc):
+    # k = 1 is the assignment; numpy's stable argsort on exact integer scores
+    X, C = workloads.integers(120, 60, 16, seed=3)
+    C[30:35] = C[2]                                  # ties across the index range
+    i1, s1 = orc.topk(X, C, 1)
+    ia, sa = orc.assign(X, C)
+    assert np.array_equal(i1[:, 0], ia) and np.array_equal(s1[:, 0], sa)
+    xs = X.to(torch.float64).numpy()
+    cs = C.to(torch.float64).numpy()
+    S = (cs * cs).sum(1)[None, :] - 2.0 * (xs @ cs.T)
+    ik, sk = orc.topk(X, C, 7)
+    exp = np.argsort(S, axis=1, kind="stable")[:, :7]
+    assert np.array_equal(ik, exp)
+    assert np.array_equal(sk, np.take_along_axis(S, exp, 1))
+    # an all-NaN row: the k lowest indices, every score NaN
+    X2, C2 = workloads.integers(2, 9, 5, seed=8, lo=-1, hi=1)
+    X2[0, 2] = math.nan
+    ik, sk = orc.topk(X2, C2, 4)
+    assert list(ik[0]) == [0, 1, 2, 3] and np.all(np.isnan(sk[0]))
+
+
+ALL_CHECKS += [check_topk_rational, check_topk_consistency]

@@ -37,6 +37,12 @@ MUTANTS = {
                                "sums[(int64_t)j * D + d] += bf16_to_double(X[i * D + (d + 1) % D]);"),
     "update_keeps_invalid_ids": ("        if (j < 0 || j >= K)\n            continue;",
                                  "        if (j < 0 || j >= K)\n            j = 0;"),
+    "topk_ties_to_higher_index": ("    return ja < jb;   /* equal scores, or both NaN */",
+                                  "    return ja > jb;   /* equal scores, or both NaN */"),
+    "topk_drops_last_slot": ("            if (pos >= k)\n                continue;",
+                             "            if (pos >= k - 1 && k > 1)\n                continue;"),
+    "topk_centroid_index_off_by_one": ("score(xi, C + j * D, cnorm[j], D)",
+                                       "score(xi, C + j * D, cnorm[j > 0 ? j - 1 : 0], D)"),
     "update_skips_first_point": ("    for (int64_t i = 0; i < N; ++i) {\n        int32_t j",
                                  "    for (int64_t i = 1; i < N; ++i) {\n        int32_t j"),
 }
