@@ -11,8 +11,9 @@ arrays into it.  Inputs are bf16 bit patterns (``numpy.uint16``), the same
 bits the CUDA path reads, so both sides see identical data.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-(exact-rational brute force, the distance identity, numpy argmin on
-integer data, hand-built cases with known answers).  The all-NaN-row
+(exact-rational brute force, the distance identity, numpy argmin and stable
+argsort on integer data, hand-built cases with known answers, the Lloyd
+descent property).  The all-NaN-row
 convention (idx 0, minscore NaN) is a documented choice, pinned by its
 definition only.
 """
@@ -70,6 +71,8 @@ def load_library(path: str):
     lib.oracle_topk.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp,
                                 ctypes.c_int64, ctypes.c_int64, vp, vp, ctypes.c_int]
     lib.oracle_topk.restype = None
+    lib.oracle_sqdist.argtypes = [vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, vp, ctypes.c_int]
+    lib.oracle_sqdist.restype = None
     return lib
 
 
@@ -212,6 +215,28 @@ def _topk(self, X, C, k, rows=None, cnorm=None, nthreads: int = 0):
     return idx, sc
 
 
+def _sqdist(self, X, C, ii, jj, nthreads: int = 0) -> np.ndarray:
+    """fp64 ||x_ii[p] - c_jj[p]||^2 for each pair, summed directly over d."""
+    X = _bits(X)
+    C = _bits(C)
+    D = X.shape[1]
+    if C.shape[1] != D:
+        raise ValueError("X and C disagree on D")
+    ii = np.ascontiguousarray(ii, dtype=np.int64).ravel()
+    jj = np.ascontiguousarray(jj, dtype=np.int64).ravel()
+    if ii.shape != jj.shape:
+        raise ValueError("ii and jj must have the same shape")
+    if ii.size and (ii.min() < 0 or ii.max() >= X.shape[0]
+                    or jj.min() < 0 or jj.max() >= C.shape[0]):
+        raise IndexError("pair index out of range")
+    out = np.empty(ii.size, dtype=np.float64)
+    if ii.size:
+        self.lib.oracle_sqdist(_ptr(X), _ptr(C), D, _ptr(ii), _ptr(jj), ii.size, _ptr(out),
+                               int(nthreads))
+    return out
+
+
+Oracle.sqdist = _sqdist
 Oracle.topk = _topk
 Oracle.update = _update
 Oracle.centroids = _centroids
@@ -243,3 +268,7 @@ def topk(X, C, k, rows=None, cnorm=None, nthreads: int = 0):
 
 def centroids(X, idx, C_old):
     return default().centroids(X, idx, C_old)
+
+
+def sqdist(X, C, ii, jj, nthreads: int = 0):
+    return default().sqdist(X, C, ii, jj, nthreads=nthreads)

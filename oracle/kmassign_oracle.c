@@ -226,3 +226,25 @@ void oracle_topk(const uint16_t *X, const uint16_t *C, const double *cnorm, int6
         }
     }
 }
+
+/*
+ * The true squared Euclidean distance ||x_i - c_j||^2 = sum_d (x_id - c_jd)^2
+ * (fp64, sequential in d) for each pair (ii[p], jj[p]): the textbook
+ * definition, written without the norm expansion the assignment uses.
+ */
+void oracle_sqdist(const uint16_t *X, const uint16_t *C, int64_t D, const int64_t *ii,
+                   const int64_t *jj, int64_t npairs, double *out, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t p = 0; p < npairs; ++p) {
+        const uint16_t *x = X + ii[p] * D;
+        const uint16_t *c = C + jj[p] * D;
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+            double diff = bf16_to_double(x[d]) - bf16_to_double(c[d]);
+            acc += diff * diff;
+        }
+        out[p] = acc;
+    }
+}

@@ -333,3 +333,32 @@ def check_topk_consistency(orc):
 
 
 ALL_CHECKS += [check_topk_rational, check_topk_consistency]
+
+
+# ---------------------------------------------------------------- squared distance
+def check_sqdist(orc):
+    # exact rational brute force of sum_d (x_d - c_d)^2
+    for t in range(6):
+        X, C = workloads.iid(5, 6, 3 + 5 * t, seed=70 + t)
+        Xf, Cf = _exact(X), _exact(C)
+        ii = np.repeat(np.arange(5), 6)
+        jj = np.tile(np.arange(6), 5)
+        got = orc.sqdist(X, C, ii, jj)
+        for p, (i, j) in enumerate(zip(ii, jj)):
+            exact = sum((a - b) ** 2 for a, b in zip(Xf[i], Cf[j]))
+            assert abs(Fraction(float(got[p])) - exact) <= Fraction(1, 2**45) * (1 + exact), (t, i, j)
+    # zero exactly at the point itself, positive elsewhere
+    X, _ = workloads.iid(8, 1, 32, seed=5)
+    n = np.arange(8)
+    assert np.all(orc.sqdist(X, X, n, n) == 0.0)
+    assert np.all(orc.sqdist(X, X, n, (n + 1) % 8) > 0.0)
+    # the norm expansion ||x||^2 + s agrees exactly on small integers
+    Xi, Ci = workloads.integers(40, 30, 16, seed=9)
+    ii = np.repeat(np.arange(40), 30)
+    jj = np.tile(np.arange(30), 40)
+    xs = Xi.to(torch.float64).numpy()
+    xn = (xs * xs).sum(1)
+    assert np.array_equal(orc.sqdist(Xi, Ci, ii, jj), xn[ii] + orc.scores(Xi, Ci, ii, jj))
+
+
+ALL_CHECKS += [check_sqdist]

@@ -43,6 +43,11 @@ MUTANTS = {
                              "            if (pos >= k - 1 && k > 1)\n                continue;"),
     "topk_centroid_index_off_by_one": ("score(xi, C + j * D, cnorm[j], D)",
                                        "score(xi, C + j * D, cnorm[j > 0 ? j - 1 : 0], D)"),
+    "sqdist_adds_instead_of_subtracting": (
+        "double diff = bf16_to_double(x[d]) - bf16_to_double(c[d]);",
+        "double diff = bf16_to_double(x[d]) + bf16_to_double(c[d]);"),
+    "sqdist_skips_last_dimension": ("        for (int64_t d = 0; d < D; ++d) {\n            double diff",
+                                    "        for (int64_t d = 0; d + 1 < D; ++d) {\n            double diff"),
     "update_skips_first_point": ("    for (int64_t i = 0; i < N; ++i) {\n        int32_t j",
                                  "    for (int64_t i = 1; i < N; ++i) {\n        int32_t j"),
 }
