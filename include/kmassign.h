@@ -60,7 +60,7 @@ enum kmassign_status {
     KMASSIGN_ERR_CUDA = -5,          /* a CUDA runtime/driver call failed */
     KMASSIGN_ERR_TIMEOUT = -6,       /* a bounded wait inside a kernel ran out */
     KMASSIGN_ERR_NOT_DEVICE = -7,    /* a pointer is not device memory */
-    KMASSIGN_ERR_ARG = -8,           /* an invalid plan value in kmassign_ex */
+    KMASSIGN_ERR_ARG = -8,           /* an invalid plan value, k or flag */
     KMASSIGN_ERR_SCRATCH = -9        /* too large for kmassign_noalloc's static scratch */
 };
 
@@ -193,6 +193,51 @@ int kmassign_centroids(const float *sums, const int32_t *counts, const void *C_o
  */
 int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int iters,
                    int32_t *idx, void *stream);
+
+/* Largest k kmassign_topk accepts. */
+#define KMASSIGN_TOPK_MAX 32
+
+/*
+ * The k nearest centroids of every point, and optionally the true squared
+ * distances to them.  Not part of flashlib PR #22, which selects one winner
+ * per point; this widens its Summary's selection step to the k best pairs
+ * (s_ij, j) under the same order as kmassign: s_ij = ||c_j||^2 - 2 x_i . c_j
+ * ascending, NaN above every number, -0 equal to +0, the lower index first
+ * among equal scores.  k = 1 returns kmassign's idx.
+ *   X, C, cnorm, N, K, D   as in kmassign
+ *   k          1 <= k <= min(K, KMASSIGN_TOPK_MAX); N * k < 2^31
+ *   idx        device int32 [N, k] row-major, written: row i ascending
+ *   score      device fp32 [N, k] row-major, or NULL (then distances must be
+ *              0); written in idx's order:
+ *                distances == 0: s_ij as kmassign's minscore computes it
+ *                                (fp32 fma of the fp32 dot and norm, -0 as
+ *                                +0, NaN for a NaN score)
+ *                distances == 1: ||x_i||^2 + s_ij in fp32 with ||x_i||^2 the
+ *                                fp32 sum of exact bf16 squares, a negative
+ *                                result (rounding) written as 0.  For
+ *                                non-finite inputs this is the same formula,
+ *                                not the direct sum of (x_d - c_d)^2
+ * Each selection uses the fp32 scores, so points whose k-th and (k+1)-th
+ * scores lie within fp32 rounding of each other may pick either.  Temporaries
+ * (norms, ||x||^2, partial lists of split centroid ranges) come from the
+ * library's stream-ordered pool.  Errors: as kmassign; k or distances out of
+ * range returns KMASSIGN_ERR_ARG, N * k >= 2^31 KMASSIGN_ERR_SHAPE,
+ * distances == 1 with score NULL KMASSIGN_ERR_NULL.
+ */
+int kmassign_topk(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                  int64_t D, int32_t k, int32_t *idx, float *score, int32_t distances,
+                  void *stream);
+
+/*
+ * kmassign_topk with an explicit centroid split (0 = automatic; > 1 splits
+ * the K axis of every row tile into ksplit ranges whose sorted candidate
+ * lists a merge kernel combines; <= -2 splits only the last, partial wave of
+ * row tiles into -ksplit ranges; -1 returns KMASSIGN_ERR_ARG).  Every split
+ * returns the same results.  Tests use it to cover the merge path.
+ */
+int kmassign_topk_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                     int64_t D, int32_t k, int32_t *idx, float *score, int32_t distances,
+                     int32_t ksplit, void *stream);
 
 /*
  * Bound, in nanoseconds of the GPU's global timer, on every pipeline wait in

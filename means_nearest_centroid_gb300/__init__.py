@@ -75,6 +75,10 @@ def _declare(lib):
     lib.kmassign_centroids.restype = i32
     lib.kmassign_lloyd.argtypes = [vp, vp, i64, i64, i64, i32, vp, vp]
     lib.kmassign_lloyd.restype = i32
+    lib.kmassign_topk.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp, i32, vp]
+    lib.kmassign_topk.restype = i32
+    lib.kmassign_topk_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp, i32, i32, vp]
+    lib.kmassign_topk_ex.restype = i32
     lib.kmassign_set_wait_timeout.argtypes = [ctypes.c_uint64]
     lib.kmassign_set_wait_timeout.restype = i32
     lib.kmassign_check.argtypes = [vp]
@@ -212,6 +216,44 @@ def kmassign_noalloc(X, C, cnorm=None, idx=None, minscore=None, stream=None):
                                     _ptr(minscore), _stream_ptr(stream))
     _check(rc, "kmassign_noalloc")
     return idx
+
+
+def kmassign_topk(X, C, k: int, cnorm=None, idx=None, score=None, distances: bool = False,
+                  with_score: bool = True, ksplit: int = 0, stream=None):
+    """The k nearest centroids of every point: (idx int32 [N, k], score fp32 [N, k]).
+
+    Row i lists centroids in ascending score s_ij = ||c_j||^2 - 2 x_i . c_j
+    (lowest index first on ties); ``distances`` returns ||x_i||^2 + s_ij
+    instead.  ``score`` is None when ``with_score`` is false and no output
+    tensor is given.  ``ksplit`` forces a split of the centroid axis (0 =
+    automatic; see ``kmassign_topk_ex`` in ``include/kmassign.h``).
+    """
+    _need_cuda(X, "X", torch.bfloat16)
+    _need_cuda(C, "C", torch.bfloat16)
+    N, D = X.shape
+    K, D2 = C.shape
+    if D != D2:
+        raise ValueError("X and C disagree on D")
+    if cnorm is not None:
+        _need_cuda(cnorm, "cnorm", torch.float32)
+    k = int(k)
+    if idx is None:
+        idx = torch.empty((N, max(k, 0)), dtype=torch.int32, device=X.device)
+    _need_cuda(idx, "idx", torch.int32)
+    if score is None and (with_score or distances):
+        score = torch.empty((N, max(k, 0)), dtype=torch.float32, device=X.device)
+    if score is not None:
+        _need_cuda(score, "score", torch.float32)
+    lib = library()
+    if ksplit:
+        rc = lib.kmassign_topk_ex(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, k, _ptr(idx),
+                                  _ptr(score), int(bool(distances)), int(ksplit),
+                                  _stream_ptr(stream))
+    else:
+        rc = lib.kmassign_topk(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, k, _ptr(idx), _ptr(score),
+                               int(bool(distances)), _stream_ptr(stream))
+    _check(rc, "kmassign_topk")
+    return idx, score
 
 
 def kmassign_plan(N: int, K: int, D: int) -> dict:

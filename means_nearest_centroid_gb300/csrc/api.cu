@@ -51,6 +51,10 @@ int current_device_info(DeviceInfo *out)
             for (int kb = 1; kb <= 4; ++kb)
                 if (kma::assign_prepare(v, kb, static_cast<size_t>(d.smem_optin)) != cudaSuccess)
                     return KMASSIGN_ERR_CUDA;
+        for (int list = 4; list <= 32; list *= 2)
+            for (int kb = 1; kb <= 4; ++kb)
+                if (kma::topk_prepare(kb, list, static_cast<size_t>(d.smem_optin)) != cudaSuccess)
+                    return KMASSIGN_ERR_CUDA;
         cudaMemPoolProps props = {};
         props.allocType = cudaMemAllocationTypePinned;
         props.location.type = cudaMemLocationTypeDevice;
@@ -183,15 +187,24 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 // only the row tiles of the last partial wave (the rest stay whole), which
 // evens out the last wave when there are a few waves of whole row tiles.
 // force_ksplit > 0 forces a uniform split, < -1 a tail split into
-// -force_ksplit ranges.
+// -force_ksplit ranges.  topk plans the k-nearest kernel, which has one shape
+// (the 256 x 128 tile with 8 consumer warps) and its own shared-memory layout;
+// its epilogue cost per tile is data dependent and taken as the assignment's.
 int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_ksplit,
-              int force_rows, int force_nt, int force_cw, Plan *out)
+              int force_rows, int force_nt, int force_cw, bool topk, Plan *out)
 {
+    auto smem_of = [&](const kma::Variant &v, int kblocks, int stages, int xbufs) {
+        return topk ? kma::topk_smem_bytes(kblocks, stages, xbufs)
+                    : kma::assign_smem_bytes(v, kblocks, stages, xbufs);
+    };
     const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
     bool found = false;
     double best_cost = 0.0;
     Plan best{};
-    for (const auto &v : kma::kVariants) {
+    const kma::Variant *variants = topk ? &kma::kTopkVariant : kma::kVariants;
+    const int nvariants = topk ? 1 : kma::kNumVariants;
+    for (int vi = 0; vi < nvariants; ++vi) {
+        const kma::Variant &v = variants[vi];
         const int rows = (v.pair ? 2 : v.sub) * kma::kTileM;   // points per unit
         if (force_rows != 0 && force_rows != rows)
             continue;
@@ -204,7 +217,7 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const int64_t P = v.pair ? dev.pair_clusters : dev.sms;   // units run in parallel
         const size_t xbytes = static_cast<size_t>(v.sub) * kblocks * kma::kXTileBytes;
         const size_t stage_bytes = static_cast<size_t>(v.pair ? v.nt / 2 : v.nt) * 128;
-        const size_t fixed = kma::assign_smem_bytes(v, kblocks, 0, 0);
+        const size_t fixed = smem_of(v, kblocks, 0, 0);
         const size_t budget = static_cast<size_t>(dev.smem_optin);
         if (fixed + xbytes + 2 * stage_bytes > budget)
             continue;
@@ -263,7 +276,7 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
                 best.grid = static_cast<int>(std::min<int64_t>(nunits, P) * (v.pair ? 2 : 1));
                 best.stages = stages;
                 best.xbufs = xbufs;
-                best.smem = kma::assign_smem_bytes(v, kblocks, stages, xbufs);
+                best.smem = smem_of(v, kblocks, stages, xbufs);
             }
         };
         if (force_ksplit > 0) {
@@ -294,10 +307,11 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
 struct PlanKey {
     int64_t N, K, D;
     int ksplit, rows, nt, cw, dev;
+    bool topk;
     bool operator==(const PlanKey &o) const
     {
         return N == o.N && K == o.K && D == o.D && ksplit == o.ksplit && rows == o.rows &&
-               nt == o.nt && cw == o.cw && dev == o.dev;
+               nt == o.nt && cw == o.cw && dev == o.dev && topk == o.topk;
     }
 };
 constexpr int kPlanCacheSize = 64;
@@ -306,9 +320,9 @@ Plan g_plans[kPlanCacheSize];
 int g_plan_count = 0, g_plan_next = 0;
 
 int cached_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int dev_id, int ksplit,
-                int rows, int nt, int cw, Plan *out)
+                int rows, int nt, int cw, Plan *out, bool topk = false)
 {
-    const PlanKey key{N, K, D, ksplit, rows, nt, cw, dev_id};
+    const PlanKey key{N, K, D, ksplit, rows, nt, cw, dev_id, topk};
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         for (int i = 0; i < g_plan_count; ++i)
@@ -317,7 +331,7 @@ int cached_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int dev_
                 return KMASSIGN_OK;
             }
     }
-    const int rc = make_plan(N, K, D, dev, ksplit, rows, nt, cw, out);
+    const int rc = make_plan(N, K, D, dev, ksplit, rows, nt, cw, topk, out);
     if (rc != KMASSIGN_OK)
         return rc;
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -441,6 +455,92 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
         rc = KMASSIGN_ERR_CUDA;
     if (tmp_norm != nullptr && cudaFreeAsync(tmp_norm, stream) != cudaSuccess)
         rc = KMASSIGN_ERR_CUDA;
+    return rc;
+}
+
+// The k nearest centroids of every point: idx and score hold [N, k] row-major;
+// distances selects ||x||^2 + s over s for score.
+int run_topk(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
+             int k, int32_t *idx, float *score, int distances, int force_ksplit,
+             cudaStream_t stream)
+{
+    int rc = check_shape(N, K, D);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    if (k < 1 || k > KMASSIGN_TOPK_MAX || k > K || (distances != 0 && distances != 1) ||
+        force_ksplit == -1)
+        return KMASSIGN_ERR_ARG;
+    if (N * k >= (int64_t(1) << 31))
+        return KMASSIGN_ERR_SHAPE;
+    if (N == 0)
+        return KMASSIGN_OK;
+    if (X == nullptr || C == nullptr || idx == nullptr || (distances && score == nullptr))
+        return KMASSIGN_ERR_NULL;
+    if (!aligned(X, 16) || !aligned(C, 16) || (cnorm && !aligned(cnorm, 16)) || !aligned(idx, 4) ||
+        (score && !aligned(score, 4)))
+        return KMASSIGN_ERR_ALIGN;
+    const void *ptrs[5] = {X, C, cnorm, idx, score};
+    if ((rc = check_device_ptrs(ptrs, 5)) != KMASSIGN_OK)
+        return rc;
+
+    DeviceInfo dev;
+    if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
+        return rc;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    Plan plan;
+    if ((rc = cached_plan(N, K, D, dev, dev_id, force_ksplit, 0, 0, 0, &plan, true)) !=
+        KMASSIGN_OK)
+        return rc;
+    const int list = kma::topk_list_size(k);
+
+    CUtensorMap xmap, cmap;
+    if (!encode_map(&xmap, X, static_cast<uint64_t>(N), static_cast<uint64_t>(D), kma::kTileM) ||
+        !encode_map(&cmap, C, static_cast<uint64_t>(K), static_cast<uint64_t>(D),
+                    c_box_rows(plan)))
+        return KMASSIGN_ERR_CUDA;
+
+    float *tmp_norm = nullptr, *xnorm = nullptr;
+    unsigned long long *part = nullptr;
+    auto take = [&](void **ptr, size_t bytes) {
+        return cudaMallocFromPoolAsync(ptr, bytes, dev.pool, stream) == cudaSuccess;
+    };
+    if (cnorm == nullptr) {
+        if (!take(reinterpret_cast<void **>(&tmp_norm), static_cast<size_t>(K) * 4))
+            return KMASSIGN_ERR_CUDA;
+        if (kma::launch_norms(C, K, D, tmp_norm, stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+        cnorm = tmp_norm;
+    }
+    if (rc == KMASSIGN_OK && distances) {
+        if (!take(reinterpret_cast<void **>(&xnorm), static_cast<size_t>(N) * 4) ||
+            kma::launch_norms(X, N, D, xnorm, stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+    }
+    const int64_t row_split = split_first_row(plan);
+    const int64_t n_split = plan.ksplit > 1 ? N - row_split : 0;
+    if (rc == KMASSIGN_OK && n_split > 0 &&
+        !take(reinterpret_cast<void **>(&part),
+              static_cast<size_t>(n_split) * plan.ksplit * list * 8))
+        rc = KMASSIGN_ERR_CUDA;
+    if (rc == KMASSIGN_OK) {
+        AssignParams p = make_params(plan, cnorm, idx, score, part, N, K, D);
+        p.topk = k;
+        p.xnorm = xnorm;
+        if (kma::launch_topk(p.kblocks, list, p, xmap, cmap, plan.grid, plan.smem, stream) !=
+            cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+        else if (part != nullptr &&
+                 kma::launch_topk_merge(list, part, n_split, plan.ksplit, k,
+                                        xnorm ? xnorm + row_split : nullptr, idx + row_split * k,
+                                        score ? score + row_split * k : nullptr,
+                                        stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+    }
+    for (void *t : {static_cast<void *>(part), static_cast<void *>(xnorm),
+                    static_cast<void *>(tmp_norm)})
+        if (t != nullptr && cudaFreeAsync(t, stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
     return rc;
 }
 
@@ -638,11 +738,11 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
     if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
     Plan plan;
-    if ((rc = make_plan(N, K, D, dev, 0, 0, 0, 0, &plan)) != KMASSIGN_OK)
+    if ((rc = make_plan(N, K, D, dev, 0, 0, 0, 0, false, &plan)) != KMASSIGN_OK)
         return rc;
     // Keys for more points than the array holds: plan without a split.
     if (plan.ksplit > 1 && N - split_first_row(plan) > kNoAllocKeyMax &&
-        (rc = make_plan(N, K, D, dev, 1, 0, 0, 0, &plan)) != KMASSIGN_OK)
+        (rc = make_plan(N, K, D, dev, 1, 0, 0, 0, false, &plan)) != KMASSIGN_OK)
         return rc;
 
     CUtensorMap xmap, cmap;
@@ -724,6 +824,22 @@ int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int
                       centroids_per_tile, consumer_warps, static_cast<cudaStream_t>(stream));
 }
 
+int kmassign_topk(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                  int64_t D, int32_t k, int32_t *idx, float *score, int32_t distances,
+                  void *stream)
+{
+    return run_topk(X, C, cnorm, N, K, D, k, idx, score, distances, 0,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int kmassign_topk_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                     int64_t D, int32_t k, int32_t *idx, float *score, int32_t distances,
+                     int32_t ksplit, void *stream)
+{
+    return run_topk(X, C, cnorm, N, K, D, k, idx, score, distances, ksplit,
+                    static_cast<cudaStream_t>(stream));
+}
+
 int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9)
 {
     if (out9 == nullptr)
@@ -735,7 +851,8 @@ int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9)
     if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
     Plan plan;
-    if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, 0, 0, 0, 0, &plan)) != KMASSIGN_OK)
+    if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, 0, 0, 0, 0, false, &plan)) !=
+        KMASSIGN_OK)
         return rc;
     out9[0] = plan.ksplit;
     out9[1] = (plan.v.pair ? 2 : plan.v.sub) * kma::kTileM;
@@ -759,10 +876,11 @@ int kmassign_check(void *stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return KMASSIGN_ERR_CUDA;
-    int code = 0;
-    if (kma::status_read_and_clear(&code) != cudaSuccess)
+    int code = 0, code_topk = 0;
+    if (kma::status_read_and_clear(&code) != cudaSuccess ||
+        kma::topk_status_read_and_clear(&code_topk) != cudaSuccess)
         return KMASSIGN_ERR_CUDA;
-    return code;
+    return code != 0 ? code : code_topk;
 }
 
 const char *kmassign_strerror(int code)
@@ -787,8 +905,9 @@ const char *kmassign_strerror(int code)
     case KMASSIGN_ERR_SCRATCH:
         return "kmassign_noalloc: K exceeds its static norm buffer (cnorm NULL needs K <= 1048576)";
     case KMASSIGN_ERR_ARG:
-        return "invalid plan value (ksplit != -1, rows_per_cta 128/256, centroids_per_tile "
-               "128/256, consumer_warps 4/8/16 matching a compiled shape)";
+        return "invalid argument (plan values: ksplit != -1, rows_per_cta 128/256, "
+               "centroids_per_tile 128/256, consumer_warps 4/8/16 matching a compiled shape; "
+               "top-k: 1 <= k <= min(K, 32), distances 0 or 1)";
     default:
         return "unknown kmassign status code";
     }

@@ -6,7 +6,8 @@
 // norms are applied (s = ||c||^2 - 2 x.c) and the winning centroid is
 // selected with lowest-index tie breaking.
 //
-// Roles inside one thread block (one block per SM, persistent):
+// Roles inside one thread block (one block per SM, persistent; the first four
+// are shared with the k-nearest kernel and live in pipeline.cuh):
 //   * X warp         - TMA-loads the block's X tile once per work unit (the
 //                      tile stays resident while centroids stream past it);
 //   * producer warp  - streams C k-blocks through a ring of shared-memory
@@ -58,129 +59,10 @@
 // warps skip their work but keep meeting their named barrier, the producer
 // waits (again bounded) for its copies in flight, the MMA warp waits for its
 // MMAs, and the tensor memory is freed before the block returns.
-#include "internal.h"
-#include "ptx.cuh"
-
-#include "kmassign.h"
+#include "pipeline.cuh"
 
 namespace kma {
-
-__device__ int g_status_word = 0;
-
 namespace {
-
-// Barrier slots (8 bytes each) after the operand and staging buffers.
-constexpr int kBarXFull = 0;                          // [kMaxXBufs]
-constexpr int kBarXEmpty = kBarXFull + kMaxXBufs;     // [kMaxXBufs]
-constexpr int kBarAccFull = kBarXEmpty + kMaxXBufs;   // [2]
-constexpr int kBarAccEmpty = kBarAccFull + 2;         // [2]
-constexpr int kBarDrain = kBarAccEmpty + 2;           // [1]
-constexpr int kBarCFull = kBarDrain + 1;              // [kMaxStages]
-constexpr int kBarCEmpty = kBarCFull + kMaxStages;    // [kMaxStages]
-constexpr int kCnStages = 4;                          // centroid-norm ring depth
-constexpr int kBarCnFull = kBarCEmpty + kMaxStages;   // [kCnStages]
-constexpr int kBarCnEmpty = kBarCnFull + kCnStages;   // [kCnStages]
-constexpr int kNumBars = kBarCnEmpty + kCnStages;
-constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot + abort flag
-constexpr uint32_t kConsumerBarrier = 1;              // named barrier id
-// Bound on the teardown waits after an abort (copies and MMAs in flight
-// always finish; this only guards against a hardware failure).
-constexpr uint64_t kDrainLimitNs = 2000000000ull;
-
-__device__ __forceinline__ void record_timeout()
-{
-    atomicCAS(&g_status_word, 0, static_cast<int>(KMASSIGN_ERR_TIMEOUT));
-}
-
-// Slow path of a bounded wait (the phase was not complete on first try).
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                       uint64_t limit_ns, bool honour_abort)
-{
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (honour_abort && *abort_flag)
-            return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
-            *abort_flag = 1u;
-            record_timeout();
-            return false;
-        }
-    }
-}
-
-// Single-thread bounded wait.  Returns false on timeout or block abort.
-__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                      uint64_t limit_ns, bool honour_abort = true)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    return wait_slow(bar, parity, abort_flag, limit_ns, honour_abort);
-}
-
-// Whole-warp bounded wait; the decision is uniform across the warp.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
-                                          volatile uint32_t *abort_flag, uint64_t limit_ns,
-                                          bool honour_abort = true)
-{
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
-        return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
-            return true;
-        int give_up = 0;
-        if ((threadIdx.x & 31) == 0) {
-            if (honour_abort && *abort_flag) {
-                give_up = 1;
-            } else if (globaltimer_ns() - t0 > limit_ns) {
-                *abort_flag = 1u;
-                record_timeout();
-                give_up = 1;
-            }
-        }
-        if (__shfl_sync(0xffffffffu, give_up, 0))
-            return false;
-    }
-}
-
-struct Unit {
-    int32_t row0;      // first point of the row tile
-    int32_t nsub;      // 128-point sub-tiles holding at least one point
-    int32_t t_begin;   // first centroid tile
-    int32_t t_end;     // one past the last centroid tile
-    bool split;        // part of a split centroid range: merge through the keys
-};
-
-// Units [0, full_units) cover one row tile and every centroid tile; the
-// remaining units split the row tiles from split_row0 on into ksplit
-// centroid ranges (all of them when full_units == 0, only the last, partial
-// wave of row tiles when the plan balances the wave tail).
-template <int SUB>
-__device__ __forceinline__ Unit decode_unit(const AssignParams &p, int u)
-{
-    Unit w;
-    int rt;
-    if (u < p.full_units) {
-        rt = u;
-        w.t_begin = 0;
-        w.t_end = p.ntiles;
-        w.split = false;
-    } else {
-        const int v = u - p.full_units;
-        const int r = v / p.ksplit;
-        const int kc = v - r * p.ksplit;
-        rt = p.split_row0 + r;
-        w.t_begin = kc * p.chunk_tiles;
-        w.t_end = min(p.ntiles, w.t_begin + p.chunk_tiles);
-        w.split = true;
-    }
-    w.row0 = rt * SUB * kTileM;
-    const int left = p.N - w.row0;
-    w.nsub = min(SUB, (left + kTileM - 1) / kTileM);
-    return w;
-}
 
 // Ordered key: fp32 score bits mapped so unsigned order == numeric order,
 // -0 folded onto +0, index in the low word.
@@ -191,31 +73,6 @@ __device__ __forceinline__ unsigned long long pack_key(float s, int j)
         u = 0u;
     const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     return (static_cast<unsigned long long>(o) << 32) | static_cast<uint32_t>(j);
-}
-
-__device__ __forceinline__ float chunk_min(const float (&s)[32])
-{
-    float a[11];
-#pragma unroll
-    for (int i = 0; i < 10; ++i)
-        a[i] = min3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-    a[10] = min2(s[30], s[31]);
-    const float b0 = min3(a[0], a[1], a[2]);
-    const float b1 = min3(a[3], a[4], a[5]);
-    const float b2 = min3(a[6], a[7], a[8]);
-    const float b3 = min2(a[9], a[10]);
-    return min3(b0, b1, min2(b2, b3));
-}
-
-// s[i] = fmaf(-2, acc[i], cnorm[j0 + i]) in place, norms from shared memory.
-__device__ __forceinline__ void apply_norms(float (&v)[32], uint32_t cn_addr)
-{
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float4 c = ld_shared_v4(cn_addr + 16u * i);
-        fma2(v[4 * i + 0], v[4 * i + 1], -2.0f, -2.0f, v[4 * i + 0], v[4 * i + 1], c.x, c.y);
-        fma2(v[4 * i + 2], v[4 * i + 3], -2.0f, -2.0f, v[4 * i + 2], v[4 * i + 3], c.z, c.w);
-    }
 }
 
 // First position of m in s (m is the minimum of s, so one exists).
@@ -286,7 +143,6 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     constexpr uint32_t kXBufBytes = SUB * KB * kXTileBytes;
     constexpr uint32_t kAccCols = SUB * NT;            // columns of one accumulator stage
     constexpr uint32_t kTmemCols = 2 * kAccCols;       // two stages: 256 or 512
-    constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, NT);
     static_assert(kTmemCols <= 512, "accumulators exceed tensor memory");
     static_assert(kCW % 32 == 0 && kChunks % kGroup == 0, "column slice must be whole chunks");
 
@@ -308,27 +164,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 0) {
-        for (int b = 0; b < kMaxXBufs; ++b) {
-            mbar_init(bar(kBarXFull + b), 1);
-            mbar_init(bar(kBarXEmpty + b), 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(bar(kBarAccFull + a), 1);
-            mbar_init(bar(kBarAccEmpty + a), kConsumerWarps);
-        }
-        mbar_init(bar(kBarDrain), 1);
-        for (int s = 0; s < kMaxStages; ++s) {
-            mbar_init(bar(kBarCFull + s), 1);
-            mbar_init(bar(kBarCEmpty + s), 1);
-        }
-        for (int s = 0; s < kCnStages; ++s) {
-            mbar_init(bar(kBarCnFull + s), 32);
-            mbar_init(bar(kBarCnEmpty + s), kConsumerWarps);
-        }
-        *abort_flag = 0u;
-        fence_mbar_init();
-    }
+    if (threadIdx.x == 0)
+        init_barriers<kConsumerWarps>(bar_base, abort_flag);
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
         tmem_relinquish();
@@ -339,159 +176,14 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == kProducerWarp) {
-        if (lane == 0) {
-            tma_prefetch_desc(&xmap);
-            tma_prefetch_desc(&cmap);
-            const uint64_t pol_c = policy_evict_last();
-            uint32_t stage = 0, phase = 0;
-            uint32_t c_issued = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const Unit w = decode_unit<SUB>(p, u);
-                for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
-#pragma unroll
-                    for (int kb = 0; kb < KB; ++kb) {
-                        if (!(ok = wait1(bar(kBarCEmpty + stage), phase ^ 1u, abort_flag,
-                                         p.timeout_ns)))
-                            break;
-                        mbar_arrive_expect_tx(bar(kBarCFull + stage), kCStageBytes);
-                        tma_load_2d(c_base + stage * kCStageBytes, &cmap, bar(kBarCFull + stage),
-                                    kb * kKBlock, tile * NT, pol_c);
-                        ++c_issued;
-                        if (++stage == static_cast<uint32_t>(p.stages)) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                }
-            }
-            if (!ok) {
-                // Let every copy still in flight land before the block exits.
-                const uint32_t S = p.stages;
-                for (uint32_t n = (c_issued > S ? c_issued - S : 0); n < c_issued; ++n)
-                    wait1(bar(kBarCFull + n % S), (n / S) & 1u, abort_flag, kDrainLimitNs, false);
-            }
-        }
-        __syncwarp();
+        producer_role<SUB, NT, KB>(p, &xmap, &cmap, c_base, bar_base, abort_flag);
     } else if (warp == kXWarp) {
-        if (lane == 0) {
-            const uint64_t pol_x = policy_evict_first();
-            uint32_t x_issued = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const Unit w = decode_unit<SUB>(p, u);
-                const uint32_t xb = x_issued % p.xbufs;
-                const uint32_t xph = (x_issued / p.xbufs) & 1u;
-                if (!(ok = wait1(bar(kBarXEmpty + xb), xph ^ 1u, abort_flag, p.timeout_ns)))
-                    break;
-                mbar_arrive_expect_tx(bar(kBarXFull + xb), w.nsub * KB * kXTileBytes);
-                const uint32_t xdst = x_base + xb * kXBufBytes;
-                for (int t = 0; t < w.nsub; ++t)
-#pragma unroll
-                    for (int kb = 0; kb < KB; ++kb)
-                        tma_load_2d(xdst + (t * KB + kb) * kXTileBytes, &xmap, bar(kBarXFull + xb),
-                                    kb * kKBlock, w.row0 + t * kTileM, pol_x);
-                ++x_issued;
-            }
-            if (!ok) {
-                const uint32_t B = p.xbufs;
-                for (uint32_t n = (x_issued > B ? x_issued - B : 0); n < x_issued; ++n)
-                    wait1(bar(kBarXFull + n % B), (n / B) & 1u, abort_flag, kDrainLimitNs, false);
-            }
-        }
-        __syncwarp();
+        x_role<SUB, KB>(p, &xmap, x_base, bar_base, abort_flag);
     } else if (warp == kMmaWarp) {
-        // The whole warp walks the schedule and waits; one elected lane issues.
-        uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0;
-        bool ok = true, issued = false;
-        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-            const Unit w = decode_unit<SUB>(p, u);
-            const uint32_t xb = x_used % p.xbufs;
-            const uint32_t xph = (x_used / p.xbufs) & 1u;
-            // Operands landed by TMA are ordered by the mbarrier itself; no
-            // tcgen05 fence is needed before MMAs read them.
-            if (!(ok = wait_warp(bar(kBarXFull + xb), xph, abort_flag, p.timeout_ns)))
-                break;
-            uint64_t adesc[SUB][KB];
-#pragma unroll
-            for (int t = 0; t < SUB; ++t)
-#pragma unroll
-                for (int kb = 0; kb < KB; ++kb)
-                    adesc[t][kb] = sw128_kmajor_desc(x_base + xb * kXBufBytes +
-                                                     (t * KB + kb) * kXTileBytes);
-            for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
-                const uint32_t as = acc_used & 1u;
-                const uint32_t aph = (acc_used >> 1) & 1u;
-                if (!(ok = wait_warp(bar(kBarAccEmpty + as), aph ^ 1u, abort_flag, p.timeout_ns)))
-                    break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + as * kAccCols;
-#pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!(ok = wait_warp(bar(kBarCFull + stage), phase, abort_flag, p.timeout_ns)))
-                        break;
-                    const uint64_t cdesc = sw128_kmajor_desc(c_base + stage * kCStageBytes);
-                    if (elect_one()) {
-                        // Sub-tiles past the last point compute on stale
-                        // operands; their rows are never stored.
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-#pragma unroll
-                            for (int t = 0; t < SUB; ++t)
-                                mma_bf16(d_tmem + t * NT, adesc[t][kb] + 2u * k, cdesc + 2u * k,
-                                         kIdesc, (kb | k) != 0);
-                        mma_commit(bar(kBarCEmpty + stage));
-                    }
-                    __syncwarp();
-                    issued = true;
-                    if (++stage == static_cast<uint32_t>(p.stages)) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok)
-                    break;
-                if (elect_one())
-                    mma_commit(bar(kBarAccFull + as));
-                __syncwarp();
-                ++acc_used;
-            }
-            if (!ok)
-                break;
-            if (elect_one())
-                mma_commit(bar(kBarXEmpty + xb));
-            __syncwarp();
-            ++x_used;
-        }
-        if (issued) {
-            // All MMAs (and the arrivals they signal) finish before teardown.
-            if (elect_one())
-                mma_commit(bar(kBarDrain));
-            __syncwarp();
-            wait_warp(bar(kBarDrain), 0u, abort_flag, kDrainLimitNs, false);
-        }
+        mma_role<SUB, NT, KB>(p, x_base, c_base, bar_base, tmem_base, abort_flag);
     } else if (warp == kNormWarp) {
-        // Norm warp: one ring slot per tile of this block's schedule.
-        float *const cn_smem = reinterpret_cast<float *>(sbase + (cn_base - base));
-        const float kNaN = __int_as_float(0x7fc00000);
-        uint32_t n = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-            const Unit w = decode_unit<SUB>(p, u);
-            for (int tile = w.t_begin; tile < w.t_end; ++tile, ++n) {
-                const uint32_t b = n % kCnStages;
-                const uint32_t ph = (n / kCnStages) & 1u;
-                if (!(ok = wait_warp(bar(kBarCnEmpty + b), ph ^ 1u, abort_flag, p.timeout_ns)))
-                    break;
-                const int j = tile * NT;
-#pragma unroll
-                for (int e = 0; e < NT / 32; ++e) {
-                    const int i = e * 32 + lane;
-                    cn_smem[b * NT + i] = (j + i < p.K) ? __ldg(p.cnorm + j + i) : kNaN;
-                }
-                mbar_arrive(bar(kBarCnFull + b));   // release: this lane's stores
-            }
-        }
+        norm_role<SUB, NT>(p, reinterpret_cast<float *>(sbase + (cn_base - base)), bar_base,
+                           abort_flag);
     } else {
         // Consumer warp w reads TMEM lanes 32*(w%4) .. +31 of sub-tile
         // (w/4)%SUB, columns [col0, col0 + kCW) of every tile.

@@ -20,7 +20,12 @@ struct AssignParams {
     const float *cnorm;            // [K] fp32
     int32_t *idx;                  // [N] (direct store when ksplit == 1)
     float *minscore;               // [N] or nullptr (direct store when ksplit == 1)
-    unsigned long long *keys;      // packed keys of the split rows (row - split_row0 * rows per tile)
+    // Packed (ordered score << 32 | index) keys of the split rows, indexed by
+    // row - split_row0 * rows per tile: one per row for the assignment, L per
+    // (row, centroid range) for the k-nearest kernel.
+    unsigned long long *keys;
+    int32_t topk;                  // k of the k-nearest kernel (idx, minscore hold [N, k])
+    const float *xnorm;            // [N] ||x||^2: the k-nearest kernel writes distances
     int32_t N, K, D;
     int32_t ksteps;                // D / 16 tensor-core k-steps
     int32_t kblocks;               // ceil(D / 64) swizzled k-blocks
@@ -55,6 +60,21 @@ cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
                           const CUtensorMap &xmap, const CUtensorMap &cmap, int grid,
                           size_t smem_bytes, cudaStream_t stream);
 
+// The k-nearest kernel: one shape (256 points x 128 centroids per tile), a
+// sorted list of `list` in {4, 8, 16, 32} >= k candidates per point.
+extern const Variant kTopkVariant;
+int topk_list_size(int k);
+size_t topk_smem_bytes(int kblocks, int stages, int xbufs);
+cudaError_t topk_prepare(int kblocks, int list, size_t smem_bytes);
+cudaError_t launch_topk(int kblocks, int list, const AssignParams &p, const CUtensorMap &xmap,
+                        const CUtensorMap &cmap, int grid, size_t smem_bytes, cudaStream_t stream);
+// Merge the per-range lists of `rows` split points ([rows][ksplit][list]
+// keys) into the k best; idx, score (may be NULL) and xnorm (NULL: scores,
+// else distances) point at the first split point.
+cudaError_t launch_topk_merge(int list, const unsigned long long *part, int64_t rows, int ksplit,
+                              int k, const float *xnorm, int32_t *idx, float *score,
+                              cudaStream_t stream);
+
 cudaError_t launch_norms(const void *C, int64_t K, int64_t D, float *cnorm, cudaStream_t stream);
 cudaError_t launch_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
                           float *sums, int32_t *counts, int sms, cudaStream_t stream);
@@ -63,7 +83,9 @@ cudaError_t launch_centroids(const float *sums, const int32_t *counts, const voi
 cudaError_t launch_finalize(const unsigned long long *keys, int64_t N, int32_t *idx,
                             float *minscore, cudaStream_t stream);
 
-// Read and clear the device status word (0 or a kmassign_status code).
+// Read and clear the device status word of the assignment kernels, and of
+// the k-nearest kernels (0 or a kmassign_status code).
 cudaError_t status_read_and_clear(int *code);
+cudaError_t topk_status_read_and_clear(int *code);
 
 }  // namespace kma

@@ -87,3 +87,79 @@ def compare(X, C, gpu_idx, gpu_ms, rows=None, integer=False, orc=None, nthreads=
         close = np.abs(g_ms - s_g) <= TOL * scale
         ms_bad = int(np.sum(~(both_nan | same_inf | (np.isfinite(s_g) & close))))
     return Report(len(rows), int(diff.sum()), rejected, ms_bad, worst)
+
+
+# ---------------------------------------------------------------- top-k
+@dataclasses.dataclass
+class TopkReport:
+    rows: int
+    invalid: int            # rows with an index out of range or repeated
+    order_bad: int          # rows whose exact scores stray from the oracle's order statistics
+    score_bad: int          # reported scores/distances outside the rule
+    unsorted: int           # rows whose reported values are not ascending
+    idx_mismatches: int     # rows whose idx list differs from the oracle's
+
+    def ok(self) -> bool:
+        return self.invalid == 0 and self.order_bad == 0 and self.score_bad == 0 and self.unsorted == 0
+
+
+def compare_topk(X, C, gpu_idx, gpu_score, k, rows=None, integer=False, distances=False,
+                 orc=None, nthreads=0) -> TopkReport:
+    """Check the GPU's k nearest centroids for ``rows`` against the oracle.
+
+    * integer data: every fp32 step is exact, so idx must equal the oracle's
+      lists and the values its scores (or direct squared distances);
+    * float data: the GPU ranks by fp32 scores within TOL * scale of the exact
+      ones (scale = ||x||^2 + max_j ||c_j||^2), so the exact score of its e-th
+      pick must lie within 2 * TOL * scale of the oracle's e-th smallest score
+      (order statistics move by at most the uniform error); each reported
+      value within TOL (scores) or 2 TOL (distances, which add the fp32
+      ||x||^2) times ||x||^2 + ||c||^2 of the exact one.
+    Every row must hold k distinct valid indices with non-decreasing values.
+    """
+    orc = orc or oracle.default()
+    gi = _as_np(gpu_idx).astype(np.int64).reshape(-1, k)
+    gs = None if gpu_score is None else _as_np(gpu_score).astype(np.float64).reshape(-1, k)
+    N, K = X.shape[0], C.shape[0]
+    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    cn64 = orc.norms(C, nthreads)
+    o_idx, o_s = orc.topk(X, C, k, rows=rows, cnorm=cn64, nthreads=nthreads)
+    g = gi[rows]
+    sg = None if gs is None else gs[rows]
+    bad_range = np.any((g < 0) | (g >= K), axis=1)
+    srt = np.sort(g, axis=1)
+    repeated = np.any(srt[:, 1:] == srt[:, :-1], axis=1) if k > 1 else np.zeros(len(rows), bool)
+    invalid = bad_range | repeated
+    n = len(rows)
+    if invalid.any():
+        return TopkReport(n, int(invalid.sum()), 0, 0, 0, n)
+    mism = int(np.sum(np.any(g != o_idx, axis=1)))
+    rr = np.repeat(rows, k)
+    exact_s = orc.scores(X, C, rr, g.ravel(), cnorm=cn64, nthreads=nthreads).reshape(-1, k)
+    exact_v = (orc.sqdist(X, C, rr, g.ravel(), nthreads=nthreads).reshape(-1, k)
+               if distances else exact_s)
+    unsorted = 0
+    if sg is not None and k > 1:
+        a, b = sg[:, :-1], sg[:, 1:]
+        ok_pair = (a <= b) | np.isnan(b) | (np.isnan(a) & np.isnan(b))
+        unsorted = int(np.sum(~np.all(ok_pair, axis=1)))
+    if integer:
+        order_bad = mism
+        score_bad = 0
+        if sg is not None:
+            same = (sg == exact_v) | (np.isnan(sg) & np.isnan(exact_v))
+            score_bad = int(np.sum(~np.all(same, axis=1)))
+        return TopkReport(n, 0, order_bad, score_bad, unsorted, mism)
+    xs = X.to(torch.float64).numpy()[rows]
+    xn = np.einsum("rd,rd->r", xs, xs)
+    scale = xn + cn64.max()
+    fin = np.isfinite(o_s) & np.isfinite(exact_s)
+    close = np.abs(exact_s - o_s) <= 2 * TOL * scale[:, None]
+    order_bad = int(np.sum(~np.all(np.where(fin, close, g == o_idx), axis=1)))
+    score_bad = 0
+    if sg is not None:
+        pair_scale = xn[:, None] + cn64[g]
+        tol = (2 * TOL if distances else TOL) * pair_scale
+        good = (np.abs(sg - exact_v) <= tol) | (np.isnan(sg) & np.isnan(exact_v))
+        score_bad = int(np.sum(~np.all(good, axis=1)))
+    return TopkReport(n, 0, order_bad, score_bad, unsorted, mism)

@@ -35,7 +35,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["kmassign", "kmassign_norms", "kmassign_ex", "kmassign_plan", "kmassign_check",
-              "kmassign_strerror"]:
+              "kmassign_strerror", "kmassign_topk", "kmassign_topk_ex"]:
         assert n in names
 
 
@@ -106,6 +106,29 @@ def test_norms_argument_errors(lib):
     assert lib.kmassign_norms(NULL, 4, 64, A16B, NULL) == S["KMASSIGN_ERR_NULL"]
     assert lib.kmassign_norms(A16, 4, 64, NULL, NULL) == S["KMASSIGN_ERR_NULL"]
     assert lib.kmassign_norms(MIS, 4, 64, A16B, NULL) == S["KMASSIGN_ERR_ALIGN"]
+
+
+def topk(lib, X=A16, C=A16B, cn=NULL, N=10, K=5, D=64, k=3, idx=A16, sc=NULL, dist=0, ksplit=None):
+    if ksplit is None:
+        return lib.kmassign_topk(X, C, cn, N, K, D, k, idx, sc, dist, NULL)
+    return lib.kmassign_topk_ex(X, C, cn, N, K, D, k, idx, sc, dist, ksplit, NULL)
+
+
+def test_topk_argument_errors(lib):
+    S = km.STATUS
+    for k in (0, -1, 6, 33):                       # k in [1, min(K, 32)]
+        assert topk(lib, k=k, K=5) == S["KMASSIGN_ERR_ARG"], k
+    assert topk(lib, k=33, K=100) == S["KMASSIGN_ERR_ARG"]
+    assert topk(lib, dist=2) == S["KMASSIGN_ERR_ARG"]
+    assert topk(lib, ksplit=-1) == S["KMASSIGN_ERR_ARG"]
+    assert topk(lib, N=2**26, k=32, K=64) == S["KMASSIGN_ERR_SHAPE"]     # N * k >= 2^31
+    assert topk(lib, D=40) == S["KMASSIGN_ERR_UNSUPPORTED_D"]
+    assert topk(lib, N=0, X=NULL, idx=NULL) == 0
+    assert topk(lib, X=NULL) == S["KMASSIGN_ERR_NULL"]
+    assert topk(lib, idx=NULL) == S["KMASSIGN_ERR_NULL"]
+    assert topk(lib, dist=1, sc=NULL) == S["KMASSIGN_ERR_NULL"]      # distances need an output
+    assert topk(lib, X=MIS) == S["KMASSIGN_ERR_ALIGN"]
+    assert topk(lib, sc=P(0x10002)) == S["KMASSIGN_ERR_ALIGN"]
 
 
 def test_plan_rejects_null_output(lib):

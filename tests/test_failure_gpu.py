@@ -50,3 +50,24 @@ def test_short_wait_bound_reports_timeout_and_context_survives(dev, plan):
     rows = list(range(0, 40000, 97)) + list(range(39700, 40000))
     rep = parity.compare(X, C, idx.cpu(), ms.cpu(), rows=sorted(set(rows)))
     assert rep.ok(), rep
+
+
+@pytest.mark.parametrize("ksplit", [0, 4])
+def test_topk_short_wait_bound_reports_timeout(dev, ksplit):
+    """The k-nearest kernel shares the bounded pipeline: same behaviour."""
+    X, C = workloads.iid(40000, 3000, 128, seed=22)
+    Xd, Cd = X.to(dev), C.to(dev)
+    assert km.kmassign_check() == 0
+    try:
+        km.kmassign_set_wait_timeout(100)
+        km.kmassign_topk(Xd, Cd, 8, ksplit=ksplit)
+        rc = km.kmassign_check()
+    finally:
+        km.kmassign_set_wait_timeout(0)
+    assert rc == km.STATUS["KMASSIGN_ERR_TIMEOUT"], km.kmassign_strerror(rc)
+    assert km.kmassign_check() == 0
+    idx, sc = km.kmassign_topk(Xd, Cd, 8, ksplit=ksplit)
+    assert km.kmassign_check() == 0
+    rows = sorted(set(range(0, 40000, 211)) | set(range(39800, 40000)))
+    rep = parity.compare_topk(X, C, idx.cpu(), sc.cpu(), 8, rows=rows)
+    assert rep.ok(), rep
