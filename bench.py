@@ -393,6 +393,60 @@ def run_update_bench(device, key, steps, warmup):
     return 0
 
 
+def run_topk_bench(device, key, ks, steps, warmup, distances=False):
+    """The k-nearest call (kmassign_topk) for each k in ``ks`` on a workload,
+    beside the assignment (kmassign) on the same three rotating input sets,
+    norms precomputed so both times are the kernel calls.  One JSON line per k;
+    the roofline is the tensor-pipe bound of the same 2*N*K*D contraction."""
+    import means_nearest_centroid_gb300 as km
+    w = workloads.WORKLOADS[key]
+    N, D, K = w.N, w.D, w.K
+    stream = torch.cuda.current_stream(device)
+    sets = []
+    for v in range(3):
+        X, C = workloads.make(key, variant=v)
+        Xd, Cd = X.to(device), C.to(device)
+        sets.append((Xd, Cd, km.kmassign_norms(Cd, stream=stream)))
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
+    def timed(call):
+        for i in range(warmup):
+            call(*sets[i % 3])
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            evs[i][0].record(stream)
+            call(*sets[i % 3])
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    idx1 = torch.empty(N, dtype=torch.int32, device=device)
+    base_ms = timed(lambda Xd, Cd, cn: km.kmassign(Xd, Cd, cnorm=cn, idx=idx1, stream=stream))
+    flops = 2.0 * N * K * D
+    for k in ks:
+        idx = torch.empty((N, k), dtype=torch.int32, device=device)
+        sc = torch.empty((N, k), dtype=torch.float32, device=device)
+        ms = timed(lambda Xd, Cd, cn: km.kmassign_topk(Xd, Cd, k, cnorm=cn, idx=idx, score=sc,
+                                                       distances=distances, stream=stream))
+        rc = km.kmassign_check(stream)
+        tf = flops / (ms * 1e-3) / 1e12
+        line = {"metric": "k nearest centroids, TFLOP/s of the score contraction",
+                "value": tf, "unit": "TFLOP/s", "k": k, "distances": distances,
+                "ms": ms, "assign_ms": base_ms, "vs_assign": base_ms / ms,
+                "steps": steps, "warmup": warmup, "higher_is_better": True,
+                "dtype": "bf16 in, fp32 scores", "data": "synthetic", "status": rc,
+                "config": {"workload": w.text, "key": key, "N": N, "D": D, "K": K,
+                           "l2": "3 rotating input sets"},
+                "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                             "frac": tf / peak, "peak_source": f"{src} bf16 burst"}}
+        print(json.dumps(line), flush=True)
+        del idx, sc
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -408,6 +462,10 @@ def main():
                     help="time the pages' 13 benchmark shapes instead (context table)")
     ap.add_argument("--update", action="store_true",
                     help="time the update step and a Lloyd iteration instead")
+    ap.add_argument("--topk", default=None,
+                    help="comma-separated k values: time the k-nearest call instead")
+    ap.add_argument("--distances", action="store_true",
+                    help="with --topk: write squared distances instead of scores")
     ap.add_argument("--parity-rows", type=int, default=256)
     ap.add_argument("--N", type=int, default=None, help="override the workload's N")
     ap.add_argument("--K", type=int, default=None, help="override the workload's K")
@@ -424,11 +482,14 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    if args.pages_shapes or args.update:
+    if args.pages_shapes or args.update or args.topk:
         from means_nearest_centroid_gb300 import _build
         _build.build()
         if args.pages_shapes:
             return run_pages_shapes(device)
+        if args.topk:
+            ks = [int(v) for v in args.topk.split(",")]
+            return run_topk_bench(device, key, ks, args.steps, args.warmup, args.distances)
         return run_update_bench(device, key, args.steps, args.warmup)
     if ws > 1:
         import torch.distributed as dist

@@ -217,6 +217,7 @@ int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int 
  *                                result (rounding) written as 0.  For
  *                                non-finite inputs this is the same formula,
  *                                not the direct sum of (x_d - c_d)^2
+ * k = 1 runs the assignment kernel (then adds ||x_i||^2 for distances).
  * Each selection uses the fp32 scores, so points whose k-th and (k+1)-th
  * scores lie within fp32 rounding of each other may pick either.  Temporaries
  * (norms, ||x||^2, partial lists of split centroid ranges) come from the
@@ -232,8 +233,9 @@ int kmassign_topk(const void *X, const void *C, const float *cnorm, int64_t N, i
  * kmassign_topk with an explicit centroid split (0 = automatic; > 1 splits
  * the K axis of every row tile into ksplit ranges whose sorted candidate
  * lists a merge kernel combines; <= -2 splits only the last, partial wave of
- * row tiles into -ksplit ranges; -1 returns KMASSIGN_ERR_ARG).  Every split
- * returns the same results.  Tests use it to cover the merge path.
+ * row tiles into -ksplit ranges; -1 returns KMASSIGN_ERR_ARG).  k = 1 takes
+ * the assignment kernel with kmassign_ex's split.  Every split returns the
+ * same results.  Tests use it to cover the merge path.
  */
 int kmassign_topk_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
                      int64_t D, int32_t k, int32_t *idx, float *score, int32_t distances,

@@ -187,9 +187,10 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 // only the row tiles of the last partial wave (the rest stay whole), which
 // evens out the last wave when there are a few waves of whole row tiles.
 // force_ksplit > 0 forces a uniform split, < -1 a tail split into
-// -force_ksplit ranges.  topk plans the k-nearest kernel, which has one shape
-// (the 256 x 128 tile with 8 consumer warps) and its own shared-memory layout;
-// its epilogue cost per tile is data dependent and taken as the assignment's.
+// -force_ksplit ranges.  topk plans the k-nearest kernel: its one shape (256
+// x 128 tiles) and shared-memory layout; its epilogue cost per tile depends on
+// the data and is taken as the assignment's, which only matters for choosing
+// the split.
 int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_ksplit,
               int force_rows, int force_nt, int force_cw, bool topk, Plan *out)
 {
@@ -486,13 +487,30 @@ int run_topk(const void *X, const void *C, const float *cnorm, int64_t N, int64_
     DeviceInfo dev;
     if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
+    if (k == 1) {
+        // The single nearest centroid is the assignment itself.
+        if ((rc = run_assign(X, C, cnorm, N, K, D, idx, score, force_ksplit, 0, 0, 0, stream)) !=
+                KMASSIGN_OK ||
+            !distances)
+            return rc;
+        float *xnorm = nullptr;
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&xnorm), static_cast<size_t>(N) * 4,
+                                    dev.pool, stream) != cudaSuccess)
+            return KMASSIGN_ERR_CUDA;
+        if (kma::launch_norms(X, N, D, xnorm, stream) != cudaSuccess ||
+            kma::launch_add_norms(score, xnorm, N, stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+        if (cudaFreeAsync(xnorm, stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+        return rc;
+    }
     int dev_id = 0;
     cudaGetDevice(&dev_id);
+    const int list = kma::topk_list_size(k);
     Plan plan;
     if ((rc = cached_plan(N, K, D, dev, dev_id, force_ksplit, 0, 0, 0, &plan, true)) !=
         KMASSIGN_OK)
         return rc;
-    const int list = kma::topk_list_size(k);
 
     CUtensorMap xmap, cmap;
     if (!encode_map(&xmap, X, static_cast<uint64_t>(N), static_cast<uint64_t>(D), kma::kTileM) ||

@@ -271,6 +271,9 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
                         }
                     }
                 }
+                // The next unit's winners may not overwrite these before
+                // they are read.
+                named_bar_sync(kConsumerBarrier, kConsumerThreads);
             }
             const int row = w.row0 + lrow;
             if (ok && h == 0 && t < w.nsub && row < p.N) {
@@ -630,6 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                         }
                     }
                 }
+                named_bar_sync(kConsumerBarrier, 32 * kConsumerWarps);
             }
             const int row = w.row0 + static_cast<int>(rank) * kTileM + lrow;
             if (ok && h == 0 && static_cast<int>(rank) < w.nsub && row < p.N) {

@@ -172,7 +172,27 @@ __global__ void centroids_kernel(const float *__restrict__ sums, const int32_t *
     }
 }
 
+// Squared distances from the assignment's scores: d = ||x||^2 + s in fp32,
+// a negative (rounding) result written as 0, NaN kept.
+__global__ void add_norms_kernel(float *__restrict__ score, const float *__restrict__ xnorm,
+                                 int64_t N)
+{
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= N)
+        return;
+    const float d = xnorm[i] + score[i];
+    score[i] = d < 0.0f ? 0.0f : d;
+}
+
 }  // namespace
+
+cudaError_t launch_add_norms(float *score, const float *xnorm, int64_t N, cudaStream_t stream)
+{
+    const int threads = 256;
+    const int64_t blocks = (N + threads - 1) / threads;
+    add_norms_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(score, xnorm, N);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
                           float *sums, int32_t *counts, int sms, cudaStream_t stream)

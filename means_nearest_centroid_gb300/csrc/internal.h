@@ -60,8 +60,9 @@ cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
                           const CUtensorMap &xmap, const CUtensorMap &cmap, int grid,
                           size_t smem_bytes, cudaStream_t stream);
 
-// The k-nearest kernel: one shape (256 points x 128 centroids per tile), a
-// sorted list of `list` in {4, 8, 16, 32} >= k candidates per point.
+// The k-nearest kernel: one shape (256 points x 128 centroids per tile, 8
+// consumer warps), a sorted list of `list` in {4, 8, 16, 32} >= k candidates
+// per point.
 extern const Variant kTopkVariant;
 int topk_list_size(int k);
 size_t topk_smem_bytes(int kblocks, int stages, int xbufs);
@@ -80,6 +81,8 @@ cudaError_t launch_update(const void *X, const int32_t *idx, int64_t N, int64_t 
                           float *sums, int32_t *counts, int sms, cudaStream_t stream);
 cudaError_t launch_centroids(const float *sums, const int32_t *counts, const void *C_old, int64_t K,
                              int64_t D, void *C_new, float *means, cudaStream_t stream);
+// score[i] = max(xnorm[i] + score[i], 0) (NaN kept): distances from scores.
+cudaError_t launch_add_norms(float *score, const float *xnorm, int64_t N, cudaStream_t stream);
 cudaError_t launch_finalize(const unsigned long long *keys, int64_t N, int32_t *idx,
                             float *minscore, cudaStream_t stream);
 

@@ -152,13 +152,19 @@ struct TopList {
     }
 };
 
-// Offer a chunk's 32 scores (columns j0 .. j0 + 31) to the list; thr is the
-// list's last score as a float (NaN while any slot is unused or NaN, which
-// lets every column through to the exact test).
+// Offer a chunk's 32 scores (columns j0 .. j0 + 31, minimum m ignoring NaN)
+// to the list.  thr is the list's last score as a float: NaN while a slot is
+// unused or when the last entry is NaN, so !(s >= thr) lets every column
+// through to the exact test.  Behind a NaN last entry only numbers can still
+// enter (a NaN column's index is larger than every NaN held), so a chunk with
+// no number (m is NaN) returns at once: a point whose scores are all NaN
+// costs two comparisons per chunk.
 template <int L>
-__device__ __forceinline__ void admit_chunk(TopList<L> &lst, const float (&s)[32], int j0,
-                                            float &thr)
+__device__ __forceinline__ void admit_chunk(TopList<L> &lst, const float (&s)[32], float m,
+                                            int j0, float &thr)
 {
+    if (m != m && lst.o[L - 1] == kNaNOrd)
+        return;
     uint32_t mask = 0;
 #pragma unroll
     for (int e = 0; e < 32; ++e)
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c)
                             if (!(m[c] >= thr))
-                                admit_chunk<L>(lst, v[c], jg + 32 * c, thr);
+                                admit_chunk<L>(lst, v[c], m[c], jg + 32 * c, thr);
                     }
                     __syncwarp();
                     if (lane == 0)

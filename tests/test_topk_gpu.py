@@ -15,7 +15,7 @@ import workloads
 
 pytestmark = pytest.mark.gpu
 
-SPLITS = [0, 2, 3, 5, -2]
+SPLITS = [0, 2, 3, 5, -2, -3]
 # (N, K, D, k): ragged N and K, every list size (4, 8, 16, 32), k == K
 SHAPES = [(1, 1, 16, 1), (1, 3, 64, 3), (5, 7, 32, 4), (300, 130, 64, 8), (129, 257, 256, 16),
           (1000, 777, 128, 32), (2000, 1000, 48, 5), (333, 2049, 96, 10), (600, 32, 64, 32),
@@ -65,7 +65,8 @@ def test_integer_shapes_bit_exact_every_split(dev, N, K, D, k):
         assert torch.equal(idx, ref[0]) and torch.equal(sc.view(torch.int32), ref[1].view(torch.int32))
 
 
-@pytest.mark.parametrize("N,K,D,k", [(700, 300, 64, 8), (129, 2049, 256, 32), (5000, 64, 16, 4)])
+@pytest.mark.parametrize("N,K,D,k", [(700, 300, 64, 8), (129, 2049, 256, 32), (5000, 64, 16, 4),
+                                     (900, 500, 128, 1)])
 @pytest.mark.parametrize("ksplit", [0, 3])
 def test_distances(dev, N, K, D, k, ksplit):
     Xi, Ci = workloads.integers(N, K, D, seed=K + k)
@@ -120,6 +121,22 @@ def test_adversarial_ties_bit_exact(dev, k):
         idx, sc = run(dev, X, C, k, ksplit=ks)
         rep = parity.compare_topk(X, C, idx, sc, k, integer=True)
         assert rep.ok() and rep.idx_mismatches == 0, (ks, rep)
+
+
+def test_nan_rows_and_nan_centroids(dev):
+    """All-NaN rows list the lowest indices with NaN scores; a NaN centroid
+    ranks after every number; +-inf rows keep their order."""
+    X, C = workloads.integers(600, 300, 32, seed=5)
+    X[::7, 3] = float("nan")
+    X[1::11, 0] = float("inf")
+    X[2::13, 5] = float("-inf")
+    C[::17, 1] = float("nan")
+    for k in (3, 8, 20):
+        for ks in SPLITS[:4]:
+            idx, sc = run(dev, X, C, k, ksplit=ks)
+            rep = parity.compare_topk(X, C, idx, sc, k, integer=True)
+            assert rep.ok() and rep.idx_mismatches == 0, (k, ks, rep)
+    assert idx[0].tolist() == list(range(20)) and torch.all(torch.isnan(sc[0]))
 
 
 def test_descending_scores_insert_every_column(dev):
