@@ -393,18 +393,20 @@ def run_update_bench(device, key, steps, warmup):
     return 0
 
 
-def run_topk_bench(device, key, ks, steps, warmup, distances=False):
+def run_topk_bench(device, key, ks, steps, warmup, distances=False, sizes=(None, None, None)):
     """The k-nearest call (kmassign_topk) for each k in ``ks`` on a workload,
     beside the assignment (kmassign) on the same three rotating input sets,
     norms precomputed so both times are the kernel calls.  One JSON line per k;
     the roofline is the tensor-pipe bound of the same 2*N*K*D contraction."""
     import means_nearest_centroid_gb300 as km
     w = workloads.WORKLOADS[key]
-    N, D, K = w.N, w.D, w.K
+    N = sizes[0] or w.N
+    K = sizes[1] or w.K
+    D = sizes[2] or w.D
     stream = torch.cuda.current_stream(device)
     sets = []
     for v in range(3):
-        X, C = workloads.make(key, variant=v)
+        X, C = workloads.make(key, N=N, K=K, D=D, variant=v)
         Xd, Cd = X.to(device), C.to(device)
         sets.append((Xd, Cd, km.kmassign_norms(Cd, stream=stream)))
     peaks, src = load_peaks()
@@ -438,8 +440,9 @@ def run_topk_bench(device, key, ks, steps, warmup, distances=False):
                 "ms": ms, "assign_ms": base_ms, "vs_assign": base_ms / ms,
                 "steps": steps, "warmup": warmup, "higher_is_better": True,
                 "dtype": "bf16 in, fp32 scores", "data": "synthetic", "status": rc,
-                "config": {"workload": w.text, "key": key, "N": N, "D": D, "K": K,
-                           "l2": "3 rotating input sets"},
+                "config": {"workload": w.text if (N, K, D) == (w.N, w.K, w.D) else
+                           f"{key} recipe at N={N}, K={K}, D={D}", "key": key, "N": N, "D": D,
+                           "K": K, "l2": "3 rotating input sets"},
                 "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                              "frac": tf / peak, "peak_source": f"{src} bf16 burst"}}
         print(json.dumps(line), flush=True)
@@ -489,7 +492,8 @@ def main():
             return run_pages_shapes(device)
         if args.topk:
             ks = [int(v) for v in args.topk.split(",")]
-            return run_topk_bench(device, key, ks, args.steps, args.warmup, args.distances)
+            return run_topk_bench(device, key, ks, args.steps, args.warmup, args.distances,
+                                  (args.N, args.K, args.D))
         return run_update_bench(device, key, args.steps, args.warmup)
     if ws > 1:
         import torch.distributed as dist
