@@ -104,13 +104,19 @@ def load_traffic(kernel_sha: str):
     return t, t
 
 
+# The sources assign_kernel is compiled from: a stored ncu traffic record is
+# reported only while these are unchanged.
+ASSIGN_KERNEL_SOURCES = [os.path.join("means_nearest_centroid_gb300", "csrc", f)
+                         for f in ("assign.cu", "pipeline.cuh", "ptx.cuh", "internal.h")] + \
+                        [os.path.join("include", "kmassign.h")]
+
+
 def kernel_source_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "means_nearest_centroid_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode())
+    for rel in ASSIGN_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(os.path.basename(rel).encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -346,21 +352,25 @@ def run_update_bench(device, key, steps, warmup):
         sets.append((Xd, Cd, km.kmassign(Xd, Cd, stream=stream)))
     sums = torch.zeros((K, D), dtype=torch.float32, device=device)
     counts = torch.zeros(K, dtype=torch.int32, device=device)
-    for i in range(warmup):
-        Xd, Cd, idx = sets[i % 3]
-        km.kmassign_update(Xd, idx, K, sums=sums, counts=counts, stream=stream)
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    for i in range(steps):
-        Xd, Cd, idx = sets[i % 3]
-        sums.zero_()
-        counts.zero_()
-        evs[i][0].record(stream)
-        km.kmassign_update(Xd, idx, K, sums=sums, counts=counts, stream=stream)
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    upd_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    def time_update(method):
+        for i in range(warmup):
+            Xd, Cd, idx = sets[i % 3]
+            km.kmassign_update(Xd, idx, K, sums=sums, counts=counts, method=method, stream=stream)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            Xd, Cd, idx = sets[i % 3]
+            sums.zero_()
+            counts.zero_()
+            evs[i][0].record(stream)
+            km.kmassign_update(Xd, idx, K, sums=sums, counts=counts, method=method, stream=stream)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    method_ms = {"atomic": time_update(1), "sorted": time_update(2)}
+    upd_ms = time_update(0)
     peaks, src = load_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     alg_bytes = 2 * N * D + 4 * N + 8 * K * D + 4 * K
@@ -381,7 +391,7 @@ def run_update_bench(device, key, steps, warmup):
             "warmup": warmup, "higher_is_better": True, "dtype": "bf16 in, fp32 sums",
             "data": "synthetic", "status": rc,
             "config": {"workload": w.text, "key": key, "N": N, "D": D, "K": K},
-            "update_ms": upd_ms,
+            "update_ms": upd_ms, "update_ms_by_method": method_ms,
             "roofline": {"bound": "hbm", "achieved": alg_bytes / (upd_ms * 1e-3) / 1e9,
                          "peak": hbm, "unit": "GB/s",
                          "frac": alg_bytes / (upd_ms * 1e-3) / 1e9 / hbm,

@@ -175,6 +175,18 @@ int kmassign_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int
                     float *sums, int32_t *counts, void *stream);
 
 /*
+ * kmassign_update with the method forced: 0 = automatic (by N * D), 1 =
+ * atomic (every point adds its row into the sums with vector reductions; one
+ * launch), 2 = sorted (a counting sort groups the points by centroid, then
+ * runs of sorted points are summed in registers and added once per centroid
+ * met; a temporary of 8K + 4N bytes from the library's pool).  Same
+ * arguments and results as kmassign_update; another method returns
+ * KMASSIGN_ERR_ARG.  Tests use it to cover both.
+ */
+int kmassign_update_ex(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
+                       float *sums, int32_t *counts, int method, void *stream);
+
+/*
  * New centroids from kmassign_update's results: C_new[j] = bf16(sums[j] /
  * counts[j]) (fp32 division, then round to nearest even) where counts[j] > 0,
  * else C_old[j].  means (fp32 [K, D], 16-byte aligned) receives the unrounded

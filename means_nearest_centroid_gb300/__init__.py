@@ -71,6 +71,8 @@ def _declare(lib):
     lib.kmassign_plan.restype = i32
     lib.kmassign_update.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
     lib.kmassign_update.restype = i32
+    lib.kmassign_update_ex.argtypes = [vp, vp, i64, i64, i64, vp, vp, i32, vp]
+    lib.kmassign_update_ex.restype = i32
     lib.kmassign_centroids.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp]
     lib.kmassign_centroids.restype = i32
     lib.kmassign_lloyd.argtypes = [vp, vp, i64, i64, i64, i32, vp, vp]
@@ -265,11 +267,12 @@ def kmassign_plan(N: int, K: int, D: int) -> dict:
     return dict(zip(keys, list(out)))
 
 
-def kmassign_update(X, idx, K: int, sums=None, counts=None, stream=None):
+def kmassign_update(X, idx, K: int, sums=None, counts=None, method: int = 0, stream=None):
     """Per-centroid fp32 sums [K, D] and int32 counts [K] of X's rows by idx.
 
     When sums/counts are given they are accumulated into; otherwise zeroed
-    tensors are created.  Returns (sums, counts).
+    tensors are created.  ``method``: 0 automatic, 1 atomic, 2 sorted (see
+    ``kmassign_update_ex`` in ``include/kmassign.h``).  Returns (sums, counts).
     """
     _need_cuda(X, "X", torch.bfloat16)
     _need_cuda(idx, "idx", torch.int32)
@@ -282,8 +285,9 @@ def kmassign_update(X, idx, K: int, sums=None, counts=None, stream=None):
         counts = torch.zeros(K, dtype=torch.int32, device=X.device)
     _need_cuda(sums, "sums", torch.float32)
     _need_cuda(counts, "counts", torch.int32)
-    _check(library().kmassign_update(_ptr(X), _ptr(idx), N, int(K), D, _ptr(sums), _ptr(counts),
-                                     _stream_ptr(stream)), "kmassign_update")
+    _check(library().kmassign_update_ex(_ptr(X), _ptr(idx), N, int(K), D, _ptr(sums),
+                                        _ptr(counts), int(method), _stream_ptr(stream)),
+           "kmassign_update")
     return sums, counts
 
 

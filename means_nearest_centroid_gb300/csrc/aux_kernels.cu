@@ -1,4 +1,5 @@
-// aux_kernels.cu -- the centroid-norm kernel and the key-finalize kernel.
+// aux_kernels.cu -- the centroid-norm kernel, the key-finalize kernel, the
+// new-centroid kernel of the update step and the distance fix-up.
 //
 // Norms (flashlib PR #22 "Optimize Blackwell k-means assignment reduction",
 // Summary: the centroid norms applied to every score tile):
@@ -74,52 +75,6 @@ __global__ void finalize_kernel(const unsigned long long *__restrict__ keys, int
         minscore[i] = ms;
 }
 
-// The update step of a Lloyd iteration, which follows the assignment (not
-// part of flashlib PR #22, which covers the assignment; the textbook update):
-// counts[j] += |{i : idx[i] == j}|, sums[j][d] += sum of x_id over them, fp32.
-// A group of D/8 lanes takes one point: each lane widens 8 bf16 values and
-// adds them with two 16-byte vector reductions into L2.  The order in which
-// points reach a centroid is not fixed, so fp32 sums of non-integer data can
-// differ in their last bits between runs; integer-valued data whose sums stay
-// below 2^24 is exact.  Ids outside [0, K) are skipped.
-__global__ void __launch_bounds__(256)
-    update_kernel(const uint4 *__restrict__ X, const int32_t *__restrict__ idx, int64_t N,
-                  int32_t K, int32_t D, float *__restrict__ sums, int32_t *__restrict__ counts)
-{
-    const int lane = threadIdx.x & 31;
-    const int vec = D >> 3;                 // 16-byte vectors per row
-    const int per_warp = 32 / vec;          // points per warp per step; spare lanes idle
-    const int slot = lane / vec;
-    const int part = lane - slot * vec;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t i0 = warp * per_warp; i0 < N; i0 += nwarps * per_warp) {
-        const int64_t i = i0 + slot;
-        if (slot >= per_warp || i >= N)
-            continue;
-        const int32_t j = __ldg(idx + i);
-        if (j < 0 || j >= K)
-            continue;
-        if (part == 0)
-            atomicAdd(counts + j, 1);
-        const uint4 q = __ldg(X + i * vec + part);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            f[2 * e] = __uint_as_float(w[e] << 16);
-            f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-        }
-        float *dst = sums + static_cast<int64_t>(j) * D + part * 8;
-        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(f[0]),
-                     "f"(f[1]), "f"(f[2]), "f"(f[3])
-                     : "memory");
-        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4), "f"(f[4]),
-                     "f"(f[5]), "f"(f[6]), "f"(f[7])
-                     : "memory");
-    }
-}
-
 // New centroids from the sums: mean (fp32, correctly rounded division) where
 // a centroid has points, written as bf16 (round to nearest even) and, when
 // asked, as fp32; a centroid without points keeps its old value.  One thread
@@ -191,19 +146,6 @@ cudaError_t launch_add_norms(float *score, const float *xnorm, int64_t N, cudaSt
     const int threads = 256;
     const int64_t blocks = (N + threads - 1) / threads;
     add_norms_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(score, xnorm, N);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
-                          float *sums, int32_t *counts, int sms, cudaStream_t stream)
-{
-    const int threads = 256;
-    const int64_t per_block = (threads / 32) * (32 / (D / 8));
-    const int64_t want = (N + per_block - 1) / per_block;
-    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * 16));
-    update_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4 *>(X), idx, N, static_cast<int32_t>(K), static_cast<int32_t>(D),
-        sums, counts);
     return cudaGetLastError();
 }
 

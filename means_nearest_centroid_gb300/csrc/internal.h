@@ -77,8 +77,15 @@ cudaError_t launch_topk_merge(int list, const unsigned long long *part, int64_t 
                               cudaStream_t stream);
 
 cudaError_t launch_norms(const void *C, int64_t K, int64_t D, float *cnorm, cudaStream_t stream);
+// The update step: atomic (one launch, L2-atomic bound) or sorted (counting
+// sort by centroid, then run reductions; needs update_sorted_scratch_bytes of
+// device scratch, 8-byte aligned).
 cudaError_t launch_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
                           float *sums, int32_t *counts, int sms, cudaStream_t stream);
+size_t update_sorted_scratch_bytes(int64_t N, int64_t K);
+cudaError_t launch_update_sorted(const void *X, const int32_t *idx, int64_t N, int64_t K,
+                                 int64_t D, float *sums, int32_t *counts, void *scratch, int sms,
+                                 cudaStream_t stream);
 cudaError_t launch_centroids(const float *sums, const int32_t *counts, const void *C_old, int64_t K,
                              int64_t D, void *C_new, float *means, cudaStream_t stream);
 // score[i] = max(xnorm[i] + score[i], 0) (NaN kept): distances from scores.

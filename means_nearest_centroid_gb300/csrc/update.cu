@@ -1,0 +1,391 @@
+// update.cu -- the update step of a Lloyd iteration, which follows the
+// assignment (not part of flashlib PR #22, which covers the assignment; the
+// textbook update): counts[j] += |{i : idx[i] == j}| and sums[j][d] += the sum
+// of x_id over those points, in fp32.  Ids outside [0, K) are skipped.
+//
+// Two ways to form the sums:
+//   * atomic: every point adds its row into L2 with 16-byte vector
+//     reductions.  One launch, but N * D / 4 reductions: the L2 atomic units,
+//     not HBM, bound it (about a sixth of the copy bandwidth for D = 256).
+//   * sorted: a counting sort groups the points by centroid (histogram,
+//     exclusive scan, scatter of point numbers), then groups of D / 8 lanes
+//     walk runs of the sorted order, gathering each point's row (one 16-byte
+//     load per lane) into registers and adding the run's total into L2 once
+//     per centroid met.  About (N / R + K) * D / 4 reductions for runs of R
+//     points, and X is read once, row by row.
+// Either way the order in which a centroid's points are added is not fixed,
+// so fp32 sums of non-integer data can differ in their last bits between
+// runs; integer-valued data whose sums stay below 2^24 is exact.
+#include "internal.h"
+
+#include <algorithm>
+
+namespace kma {
+namespace {
+
+__device__ __forceinline__ void red_add_v4(float *dst, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void widen8(const uint4 &q, float (&f)[8])
+{
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        f[2 * e] = __uint_as_float(w[e] << 16);
+        f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+
+// Atomic form: a group of D/8 lanes takes one point at a time.
+__global__ void __launch_bounds__(256)
+    update_kernel(const uint4 *__restrict__ X, const int32_t *__restrict__ idx, int64_t N,
+                  int32_t K, int32_t D, float *__restrict__ sums, int32_t *__restrict__ counts)
+{
+    const int lane = threadIdx.x & 31;
+    const int vec = D >> 3;                 // 16-byte vectors per row
+    const int per_warp = 32 / vec;          // points per warp per step; spare lanes idle
+    const int slot = lane / vec;
+    const int part = lane - slot * vec;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t i0 = warp * per_warp; i0 < N; i0 += nwarps * per_warp) {
+        const int64_t i = i0 + slot;
+        if (slot >= per_warp || i >= N)
+            continue;
+        const int32_t j = __ldg(idx + i);
+        if (j < 0 || j >= K)
+            continue;
+        if (part == 0)
+            atomicAdd(counts + j, 1);
+        float f[8];
+        widen8(__ldg(X + i * vec + part), f);
+        float *dst = sums + static_cast<int64_t>(j) * D + part * 8;
+        red_add_v4(dst, f[0], f[1], f[2], f[3]);
+        red_add_v4(dst + 4, f[4], f[5], f[6], f[7]);
+    }
+}
+
+// ---- sorted form ----------------------------------------------------------
+
+constexpr int kScanThreads = 1024;
+constexpr int kScanPer = 4;                           // elements per thread
+constexpr int kScanTile = kScanThreads * kScanPer;    // elements per block tile
+constexpr int64_t kSmallScanMax = 65536;              // centroids scanned by one block
+
+// Points per thread in the histogram and scatter passes: their atomics are
+// independent, so a thread keeps this many in flight.
+constexpr int kPerThread = 8;
+
+// hist[j] += 1 for every point with a valid id.
+__global__ void __launch_bounds__(256)
+    hist_kernel(const int32_t *__restrict__ idx, int64_t N, int32_t K, int32_t *__restrict__ hist)
+{
+    const int64_t base = (static_cast<int64_t>(blockIdx.x) * blockDim.x) * kPerThread + threadIdx.x;
+    int32_t j[kPerThread];
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int64_t i = base + static_cast<int64_t>(u) * blockDim.x;
+        j[u] = i < N ? __ldg(idx + i) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u)
+        if (j[u] >= 0 && j[u] < K)
+            atomicAdd(hist + j[u], 1);
+}
+
+// Exclusive scan of one value per thread over a block of kScanThreads;
+// *block_total receives the sum.  Uses 32 ints of shared memory.
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t *warp_sums,
+                                                        int64_t *block_total)
+{
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    int64_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off)
+            incl += t;
+    }
+    if (lane == 31)
+        warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int64_t w = warp_sums[lane];
+        int64_t wi = w;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t t = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off)
+                wi += t;
+        }
+        warp_sums[lane] = wi - w;   // exclusive prefix of warp totals
+        if (lane == 31)
+            warp_sums[32] = wi;
+    }
+    __syncthreads();
+    const int64_t out = incl - v + warp_sums[warp];
+    *block_total = warp_sums[32];
+    __syncthreads();   // warp_sums is reused by the caller's next scan
+    return out;
+}
+
+// Phase A (many tiles only): tile_sum[b] = sum of hist over tile b.
+__global__ void __launch_bounds__(kScanThreads)
+    tile_sum_kernel(const int32_t *__restrict__ hist, int32_t K, int64_t *__restrict__ tile_sum)
+{
+    __shared__ int64_t warp_sums[33];
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kScanTile + threadIdx.x * kScanPer;
+    int64_t v = 0;
+#pragma unroll
+    for (int e = 0; e < kScanPer; ++e)
+        if (base + e < K)
+            v += hist[base + e];
+    int64_t total;
+    block_exclusive_scan(v, warp_sums, &total);
+    if (threadIdx.x == 0)
+        tile_sum[blockIdx.x] = total;
+}
+
+// Phase B (many tiles only, one block): tile_sum -> exclusive tile offsets.
+__global__ void __launch_bounds__(kScanThreads)
+    tile_offsets_kernel(int64_t *__restrict__ tile_sum, int64_t ntiles)
+{
+    __shared__ int64_t warp_sums[33];
+    int64_t carry = 0;
+    for (int64_t b0 = 0; b0 < ntiles; b0 += kScanThreads) {
+        const int64_t b = b0 + threadIdx.x;
+        const int64_t v = b < ntiles ? tile_sum[b] : 0;
+        int64_t total;
+        const int64_t ex = block_exclusive_scan(v, warp_sums, &total);
+        if (b < ntiles)
+            tile_sum[b] = carry + ex;
+        carry += total;
+    }
+}
+
+// Few centroids (K <= kSmallScanMax): one block walks the tiles in order,
+// carrying the running total (one launch instead of three).  Same outputs as
+// phase C.
+__global__ void __launch_bounds__(kScanThreads)
+    scan_small_kernel(const int32_t *__restrict__ hist, int32_t K, int32_t *__restrict__ cursor,
+                      int32_t *__restrict__ counts, int32_t *__restrict__ total_out)
+{
+    __shared__ int64_t warp_sums[33];
+    int64_t carry = 0;
+    for (int64_t t0 = 0; t0 < K; t0 += kScanTile) {
+        const int64_t base = t0 + threadIdx.x * kScanPer;
+        int32_t h[kScanPer];
+        int64_t v = 0;
+#pragma unroll
+        for (int e = 0; e < kScanPer; ++e) {
+            h[e] = base + e < K ? hist[base + e] : 0;
+            v += h[e];
+        }
+        int64_t total;
+        int64_t run = carry + block_exclusive_scan(v, warp_sums, &total);
+#pragma unroll
+        for (int e = 0; e < kScanPer; ++e) {
+            if (base + e < K) {
+                cursor[base + e] = static_cast<int32_t>(run);
+                counts[base + e] += h[e];
+            }
+            run += h[e];
+        }
+        carry += total;
+    }
+    if (threadIdx.x == 0)
+        *total_out = static_cast<int32_t>(carry);
+}
+
+// Phase C: cursor[j] = first sorted position of centroid j; counts[j] +=
+// hist[j]; the block holding the last tile writes the number of sorted points.
+__global__ void __launch_bounds__(kScanThreads)
+    scan_apply_kernel(const int32_t *__restrict__ hist, int32_t K,
+                      const int64_t *__restrict__ tile_off, int32_t *__restrict__ cursor,
+                      int32_t *__restrict__ counts, int32_t *__restrict__ total_out)
+{
+    __shared__ int64_t warp_sums[33];
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kScanTile + threadIdx.x * kScanPer;
+    int32_t h[kScanPer];
+    int64_t v = 0;
+#pragma unroll
+    for (int e = 0; e < kScanPer; ++e) {
+        h[e] = base + e < K ? hist[base + e] : 0;
+        v += h[e];
+    }
+    int64_t total;
+    int64_t run = block_exclusive_scan(v, warp_sums, &total) +
+                  (tile_off != nullptr ? tile_off[blockIdx.x] : 0);
+#pragma unroll
+    for (int e = 0; e < kScanPer; ++e) {
+        if (base + e < K) {
+            cursor[base + e] = static_cast<int32_t>(run);
+            counts[base + e] += h[e];
+        }
+        run += h[e];
+    }
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0)
+        *total_out = static_cast<int32_t>((tile_off != nullptr ? tile_off[blockIdx.x] : 0) + total);
+}
+
+// perm[cursor[j]++] = i for every point with a valid id j.
+__global__ void __launch_bounds__(256)
+    scatter_kernel(const int32_t *__restrict__ idx, int64_t N, int32_t K,
+                   int32_t *__restrict__ cursor, int32_t *__restrict__ perm)
+{
+    const int64_t base = (static_cast<int64_t>(blockIdx.x) * blockDim.x) * kPerThread + threadIdx.x;
+    int32_t j[kPerThread], pos[kPerThread];
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int64_t i = base + static_cast<int64_t>(u) * blockDim.x;
+        j[u] = i < N ? __ldg(idx + i) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u)
+        pos[u] = (j[u] >= 0 && j[u] < K) ? atomicAdd(cursor + j[u], 1) : -1;
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u)
+        if (pos[u] >= 0)
+            perm[pos[u]] = static_cast<int32_t>(base + static_cast<int64_t>(u) * blockDim.x);
+}
+
+// Runs of R sorted points per group of D/8 lanes (R a multiple of kAhead):
+// the group gathers kAhead rows at a time and adds a centroid's partial sum
+// into L2 whenever the centroid changes, and at the end of the run.
+constexpr int kAhead = 8;
+
+__global__ void __launch_bounds__(256)
+    segsum_kernel(const uint4 *__restrict__ X, const int32_t *__restrict__ perm,
+                  const int32_t *__restrict__ idx, const int32_t *__restrict__ total_p, int32_t D,
+                  int32_t R, float *__restrict__ sums)
+{
+    const int lane = threadIdx.x & 31;
+    const int vec = D >> 3;
+    const int per_warp = 32 / vec;
+    const int slot = lane / vec;
+    const int part = lane - slot * vec;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t total = *total_p;
+    const int64_t begin = (warp * per_warp + slot) * R;
+    if (slot >= per_warp || begin >= total)
+        return;   // no collective operations below
+    const int64_t end = min(begin + R, total);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int32_t cur = -1;
+    auto flush = [&]() {
+        float *dst = sums + static_cast<int64_t>(cur) * D + part * 8;
+        red_add_v4(dst, acc[0], acc[1], acc[2], acc[3]);
+        red_add_v4(dst + 4, acc[4], acc[5], acc[6], acc[7]);
+    };
+    for (int64_t s0 = begin; s0 < end; s0 += kAhead) {
+        int32_t i[kAhead], j[kAhead];
+        uint4 q[kAhead];
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u)
+            i[u] = s0 + u < end ? __ldg(perm + s0 + u) : -1;
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u)
+            j[u] = i[u] >= 0 ? __ldg(idx + i[u]) : -1;
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u)
+            if (i[u] >= 0)
+                q[u] = __ldg(X + static_cast<int64_t>(i[u]) * vec + part);
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            if (i[u] < 0)
+                break;
+            if (j[u] != cur) {
+                if (cur >= 0)
+                    flush();
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[e] = 0.f;
+                cur = j[u];
+            }
+            float f[8];
+            widen8(q[u], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] += f[e];
+        }
+    }
+    if (cur >= 0)
+        flush();
+}
+
+}  // namespace
+
+cudaError_t launch_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
+                          float *sums, int32_t *counts, int sms, cudaStream_t stream)
+{
+    const int threads = 256;
+    const int64_t per_block = (threads / 32) * (32 / (D / 8));
+    const int64_t want = (N + per_block - 1) / per_block;
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * 16));
+    update_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(X), idx, N, static_cast<int32_t>(K), static_cast<int32_t>(D),
+        sums, counts);
+    return cudaGetLastError();
+}
+
+size_t update_sorted_scratch_bytes(int64_t N, int64_t K)
+{
+    const int64_t ntiles = (K + kScanTile - 1) / kScanTile;
+    return static_cast<size_t>(K) * 4 * 2 +              // hist, cursor
+           static_cast<size_t>(N) * 4 +                  // perm
+           static_cast<size_t>(ntiles) * 8 + 64;         // tile offsets, total
+}
+
+cudaError_t launch_update_sorted(const void *X, const int32_t *idx, int64_t N, int64_t K,
+                                 int64_t D, float *sums, int32_t *counts, void *scratch, int sms,
+                                 cudaStream_t stream)
+{
+    const int64_t ntiles = (K + kScanTile - 1) / kScanTile;
+    uint8_t *p = static_cast<uint8_t *>(scratch);
+    int32_t *hist = reinterpret_cast<int32_t *>(p);
+    int32_t *cursor = hist + K;
+    int32_t *perm = cursor + K;
+    uint8_t *tail = reinterpret_cast<uint8_t *>(perm + N);
+    int64_t *tile_off = reinterpret_cast<int64_t *>(
+        (reinterpret_cast<uintptr_t>(tail) + 7) & ~uintptr_t(7));
+    int32_t *total = reinterpret_cast<int32_t *>(tile_off + ntiles);
+    cudaError_t e = cudaMemsetAsync(hist, 0, static_cast<size_t>(K) * 4, stream);
+    if (e != cudaSuccess)
+        return e;
+    const int threads = 256;
+    const int64_t blocks = (N + int64_t(threads) * kPerThread - 1) / (int64_t(threads) * kPerThread);
+    hist_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(idx, N,
+                                                                      static_cast<int32_t>(K), hist);
+    if (K <= kSmallScanMax) {
+        scan_small_kernel<<<1, kScanThreads, 0, stream>>>(hist, static_cast<int32_t>(K), cursor,
+                                                          counts, total);
+    } else {
+        tile_sum_kernel<<<static_cast<unsigned>(ntiles), kScanThreads, 0, stream>>>(
+            hist, static_cast<int32_t>(K), tile_off);
+        tile_offsets_kernel<<<1, kScanThreads, 0, stream>>>(tile_off, ntiles);
+        scan_apply_kernel<<<static_cast<unsigned>(ntiles), kScanThreads, 0, stream>>>(
+            hist, static_cast<int32_t>(K), tile_off, cursor, counts, total);
+    }
+    scatter_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        idx, N, static_cast<int32_t>(K), cursor, perm);
+    // Runs of R points: enough groups to give every SM about 48 resident warps.
+    const int vec = static_cast<int>(D / 8);
+    const int per_warp = 32 / vec;
+    const int64_t groups_target = int64_t(sms) * 48 * per_warp;
+    int64_t R = (N + groups_target - 1) / groups_target;
+    R = std::max<int64_t>(kAhead, (R + kAhead - 1) / kAhead * kAhead);
+    const int64_t groups = (N + R - 1) / R;
+    const int64_t warps = (groups + per_warp - 1) / per_warp;
+    const int64_t sblocks = (warps * 32 + threads - 1) / threads;
+    segsum_kernel<<<static_cast<unsigned>(sblocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(X), perm, idx, total, static_cast<int32_t>(D),
+        static_cast<int32_t>(R), sums);
+    return cudaGetLastError();
+}
+
+}  // namespace kma

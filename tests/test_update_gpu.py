@@ -48,25 +48,58 @@ def check_sums(X, idx, K, sums, counts, integer):
         assert np.all(np.abs(g - o_sums) <= bound), float(np.max(np.abs(g - o_sums) - bound))
 
 
+METHODS = [0, 1, 2]   # automatic, atomic, sorted
+
+
 @pytest.mark.parametrize("N,K,D", [(1, 1, 16), (1000, 37, 64), (5000, 300, 128), (3000, 17, 256),
-                                   (2048, 1000, 48), (999, 5, 80)])
-def test_update_float_and_integer(dev, N, K, D):
-    X, C = workloads.blobs(N, K, D, seed=N + D)
+                                   (2048, 1000, 48), (999, 5, 80), (20000, 5000, 96),
+                                   (9000, 70000, 16)])
+@pytest.mark.parametrize("method", METHODS)
+def test_update_float_and_integer(dev, N, K, D, method):
+    X, C = workloads.blobs(N, min(K, 4096), D, seed=N + D)
     g = np.random.default_rng(N)
     idx = g.integers(-2, K + 2, N).astype(np.int32)          # includes ids to skip
-    sums, counts = km.kmassign_update(X.to(dev), torch.from_numpy(idx).to(dev), K)
+    sums, counts = km.kmassign_update(X.to(dev), torch.from_numpy(idx).to(dev), K, method=method)
     check_sums(X, idx, K, sums, counts, integer=False)
-    Xi, _ = workloads.integers(N, K, D, seed=N * 3)
-    sums, counts = km.kmassign_update(Xi.to(dev), torch.from_numpy(idx).to(dev), K)
+    Xi, _ = workloads.integers(N, 1, D, seed=N * 3)
+    sums, counts = km.kmassign_update(Xi.to(dev), torch.from_numpy(idx).to(dev), K, method=method)
     check_sums(Xi, idx, K, sums, counts, integer=True)
 
 
-def test_update_accumulates_batches(dev):
+@pytest.mark.parametrize("method", [1, 2])
+def test_update_skewed_clusters(dev, method):
+    """Most points on a few centroids (long runs), the rest spread thinly."""
+    N, K, D = 50000, 3000, 64
+    Xi, _ = workloads.integers(N, 1, D, seed=5)
+    g = np.random.default_rng(5)
+    idx = np.where(g.random(N) < 0.8, g.integers(0, 3, N), g.integers(0, K, N)).astype(np.int32)
+    sums, counts = km.kmassign_update(Xi.to(dev), torch.from_numpy(idx).to(dev), K, method=method)
+    check_sums(Xi, idx, K, sums, counts, integer=True)
+
+
+def test_update_methods_agree_on_integers(dev):
+    X, _ = workloads.integers(30000, 1, 128, seed=6)
+    idx = torch.from_numpy(np.random.default_rng(6).integers(0, 900, 30000).astype(np.int32))
+    Xd, idxd = X.to(dev), idx.to(dev)
+    a = km.kmassign_update(Xd, idxd, 900, method=1)
+    b = km.kmassign_update(Xd, idxd, 900, method=2)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_update_rejects_unknown_method(dev):
+    X, _ = workloads.integers(10, 1, 16, seed=1)
+    idx = torch.zeros(10, dtype=torch.int32, device=dev)
+    with pytest.raises(km.KmassignError):
+        km.kmassign_update(X.to(dev), idx, 4, method=3)
+
+
+@pytest.mark.parametrize("method", METHODS)
+def test_update_accumulates_batches(dev, method):
     X, _ = workloads.integers(4000, 1, 64, seed=8)
     idx = np.random.default_rng(1).integers(0, 50, 4000).astype(np.int32)
     Xd, idxd = X.to(dev), torch.from_numpy(idx).to(dev)
-    sums, counts = km.kmassign_update(Xd[:1500], idxd[:1500], 50)
-    km.kmassign_update(Xd[1500:], idxd[1500:], 50, sums=sums, counts=counts)
+    sums, counts = km.kmassign_update(Xd[:1500], idxd[:1500], 50, method=method)
+    km.kmassign_update(Xd[1500:], idxd[1500:], 50, sums=sums, counts=counts, method=method)
     check_sums(X, idx, 50, sums, counts, integer=True)
 
 
@@ -127,10 +160,26 @@ def test_lloyd_rejects_negative_iterations(dev):
         km.kmassign_lloyd(X.to(dev), C.to(dev), iters=-1)
 
 
-def test_update_full_size_lognormal(dev):
+@pytest.mark.parametrize("method", [1, 2])
+def test_update_full_size_lognormal(dev, method):
     w = workloads.WORKLOADS["lognormal_clusters"]
     X, C = workloads.make("lognormal_clusters")
     Xd, Cd = X.to(dev), C.to(dev)
     idx = km.kmassign(Xd, Cd)
-    sums, counts = km.kmassign_update(Xd, idx, w.K)
+    sums, counts = km.kmassign_update(Xd, idx, w.K, method=method)
     check_sums(X, idx.cpu().numpy(), w.K, sums, counts, integer=False)
+
+
+def test_update_sorted_many_scan_tiles(dev):
+    """K large enough that the tile offsets take several passes of one block."""
+    N, K, D = 3000, 4_300_000, 16
+    Xi, _ = workloads.integers(N, 1, D, seed=9)
+    g = np.random.default_rng(9)
+    idx = np.concatenate([g.integers(0, K, N - 100), np.full(100, K - 1)]).astype(np.int32)
+    sums, counts = km.kmassign_update(Xi.to(dev), torch.from_numpy(idx).to(dev), K, method=2)
+    o_sums, o_counts = oracle.update(Xi, idx, K)
+    touched = np.unique(idx)
+    assert np.array_equal(counts.cpu().numpy().astype(np.int64), o_counts)
+    assert np.array_equal(sums[torch.from_numpy(touched).to(dev)].cpu().double().numpy(),
+                          o_sums[touched])
+    assert float(sums.abs().sum()) == float(np.abs(o_sums).sum())
