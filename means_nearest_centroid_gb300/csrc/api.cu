@@ -48,7 +48,7 @@ int current_device_info(DeviceInfo *out)
                 cudaSuccess)
             return KMASSIGN_ERR_CUDA;
         for (const auto &v : kma::kVariants)
-            for (int kb = 1; kb <= 4; ++kb)
+            for (int kb = v.pair ? 2 : 1; kb <= 4; ++kb)   // pair kernels: D > 64 only
                 if (kma::assign_prepare(v, kb, static_cast<size_t>(d.smem_optin)) != cudaSuccess)
                     return KMASSIGN_ERR_CUDA;
         for (int list = 4; list <= 32; list *= 2)
@@ -213,8 +213,8 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
             continue;
         if (force_cw != 0 && force_cw != 4 * v.sub * v.ch)
             continue;
-        if (v.pair && dev.pair_clusters < 1)
-            continue;
+        if (v.pair && (dev.pair_clusters < 1 || kblocks <= 1))
+            continue;   // pair kernels exist for D > 64 only
         const int64_t P = v.pair ? dev.pair_clusters : dev.sms;   // units run in parallel
         const size_t xbytes = static_cast<size_t>(v.sub) * kblocks * kma::kXTileBytes;
         const size_t stage_bytes = static_cast<size_t>(v.pair ? v.nt / 2 : v.nt) * 128;

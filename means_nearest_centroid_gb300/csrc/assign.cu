@@ -88,12 +88,14 @@ __device__ __forceinline__ int first_of(const float (&s)[32], float m)
 // Fold chunk scores s (columns j0 .. j0+31, chunk minimum m) into (best, bi).
 // SNAP: keep the chunk's scores in this thread's shared slot (float4 i of
 // thread t at slot + 512*i, conflict-free across the warp) and let bi hold the
-// chunk's first column until resolve_snapshot.
-template <bool SNAP>
+// chunk's first column until resolve_snapshot.  MAX: the values are
+// t = -s / 2 (norm-folded accumulators), so the best is the largest, and m is
+// the chunk maximum.
+template <bool SNAP, bool MAX = false>
 __device__ __forceinline__ void fold_chunk(const float (&s)[32], float m, int j0, float &best,
                                            int &bi, uint32_t slot)
 {
-    if (m < best || (m == best && bi == kNone)) {
+    if ((MAX ? m > best : m < best) || (m == best && bi == kNone)) {
         best = m;
         if (SNAP) {
 #pragma unroll
@@ -135,6 +137,14 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     constexpr int kNormWarp = kConsumerWarps + 2;
     constexpr int kXWarp = kConsumerWarps + 3;
     constexpr bool kSnap = KB <= 2;                    // D <= 128: epilogue-bound
+    // D <= 64: the norms enter the accumulator through one more MMA step
+    // (25% more tensor work at D = 64, a quarter of the reduction's
+    // instructions saved: measured 4-9% faster at D = 64 and 3-6% slower at
+    // D = 128, so only one k-block folds); the accumulator then holds
+    // t = x.c - ||c||^2 / 2 = -s / 2 and the reduction takes the largest t.
+    constexpr bool kFold = KB == 1;
+    constexpr uint32_t kNormBytes =
+        kFold ? kOnesBytes + kFoldStages * NT * 32u : kCnStages * NT * 4u;
     constexpr int kCW = NT / CH;                       // columns per consumer warp per tile
     constexpr int kChunks = kCW / 32;
     constexpr int kGroup = kChunks < 4 ? kChunks : 4;  // chunks loaded per tcgen05.wait::ld
@@ -151,8 +161,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t x_base = base;
     const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
-    const uint32_t cn_base = c_base + p.stages * kCStageBytes;       // float[kCnStages][NT]
-    const uint32_t red_base = cn_base + kCnStages * NT * 4;           // {float,int}[CH-1][SUB*128]
+    const uint32_t cn_base = c_base + p.stages * kCStageBytes;   // norm ring, or fold region
+    const uint32_t red_base = cn_base + kNormBytes;               // {float,int}[CH-1][SUB*128]
     const uint32_t snap_base = red_base + (CH - 1) * SUB * kTileM * 8;   // [warp][8][32] float4
     const uint32_t bar_base = snap_base + (kSnap ? kConsumerWarps * 4096u : 0u);
     uint8_t *const sbase = smem_raw + (base - raw);
@@ -165,7 +175,9 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0)
-        init_barriers<kConsumerWarps>(bar_base, abort_flag);
+        init_barriers<kConsumerWarps, kFold>(bar_base, abort_flag);
+    if (kFold)
+        fold_init<NT>(cn_base);
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
         tmem_relinquish();
@@ -180,10 +192,13 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     } else if (warp == kXWarp) {
         x_role<SUB, KB>(p, &xmap, x_base, bar_base, abort_flag);
     } else if (warp == kMmaWarp) {
-        mma_role<SUB, NT, KB>(p, x_base, c_base, bar_base, tmem_base, abort_flag);
+        mma_role<SUB, NT, KB, kFold>(p, x_base, c_base, bar_base, tmem_base, abort_flag, cn_base);
     } else if (warp == kNormWarp) {
-        norm_role<SUB, NT>(p, reinterpret_cast<float *>(sbase + (cn_base - base)), bar_base,
-                           abort_flag);
+        if (kFold)
+            fold_norm_role<SUB, NT>(p, cn_base, bar_base, abort_flag);
+        else
+            norm_role<SUB, NT>(p, reinterpret_cast<float *>(sbase + (cn_base - base)), bar_base,
+                               abort_flag);
     } else {
         // Consumer warp w reads TMEM lanes 32*(w%4) .. +31 of sub-tile
         // (w/4)%SUB, columns [col0, col0 + kCW) of every tile.
@@ -199,7 +214,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
 
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             const Unit w = decode_unit<SUB>(p, u);
-            float best = __int_as_float(0x7f800000);   // +inf
+            // +inf for scores, -inf for folded t
+            float best = __int_as_float(kFold ? 0xff800000 : 0x7f800000);
             int bi = kNone;
             for (int tile = w.t_begin; tile < w.t_end; ++tile, ++acc_used) {
                 const uint32_t as = acc_used & 1u;
@@ -208,7 +224,7 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
                 const uint32_t nph = (acc_used / kCnStages) & 1u;
                 if (ok)
                     ok = wait_warp(bar(kBarAccFull + as), aph, abort_flag, p.timeout_ns);
-                if (ok)
+                if (ok && !kFold)
                     ok = wait_warp(bar(kBarCnFull + nb), nph, abort_flag, p.timeout_ns);
                 if (ok) {
                     tc_fence_after();
@@ -233,23 +249,31 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
                         float m[kGroup];
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c) {
-                            apply_norms(v[c], cn_tile + 128u * (g * kGroup + c));
-                            m[c] = chunk_min(v[c]);
+                            if (kFold) {
+                                m[c] = chunk_max(v[c]);
+                            } else {
+                                apply_norms(v[c], cn_tile + 128u * (g * kGroup + c));
+                                m[c] = chunk_min(v[c]);
+                            }
                         }
                         const int jg = tile * NT + col0 + g * kGroup * 32;
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c)
-                            fold_chunk<kSnap>(v[c], m[c], jg + 32 * c, best, bi, slot);
+                            fold_chunk<kSnap, kFold>(v[c], m[c], jg + 32 * c, best, bi, slot);
                     }
-                    // This warp is done with the tile's norms.
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(bar(kBarCnEmpty + nb));
+                    if (!kFold) {
+                        // This warp is done with the tile's norms.
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(bar(kBarCnEmpty + nb));
+                    }
                 }
             }
 
             if (kSnap)
                 resolve_snapshot(best, bi, slot);
+            if (kFold)
+                best = -2.0f * best;   // t back to the score s (exact)
             // Merge the column slices of each point: (score, index) order.
             const int lrow = t * kTileM + q * 32 + lane;
             if (CH > 1) {
@@ -685,10 +709,9 @@ template <int CH>
 cudaError_t dispatch_pair_kb(bool prepare, int kb, const AssignParams *p, const CUtensorMap *xmap,
                              const CUtensorMap *cmap, int grid, size_t smem, cudaStream_t stream)
 {
+    // D <= 64 has no pair kernel: there the single-block kernels fold the
+    // norms into the MMA, and every plan must give the same bits.
     switch (kb) {
-    case 1:
-        return prepare ? prepare_pair<CH, 1>(smem)
-                       : launch_pair<CH, 1>(*p, *xmap, *cmap, grid, smem, stream);
     case 2:
         return prepare ? prepare_pair<CH, 2>(smem)
                        : launch_pair<CH, 2>(*p, *xmap, *cmap, grid, smem, stream);
@@ -774,8 +797,11 @@ const Variant kVariants[kNumVariants] = {{2, 128, 1, false}, {1, 256, 2, false},
 size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 {
     const size_t stage_rows = v.pair ? v.nt / 2 : v.nt;
+    const bool fold = !v.pair && kblocks == 1;   // the single-block kernel's kFold
+    const size_t norm_bytes =
+        fold ? kOnesBytes + static_cast<size_t>(kFoldStages) * v.nt * 32 : kCnStages * v.nt * 4;
     return 1024 + static_cast<size_t>(xbufs) * v.sub * kblocks * kXTileBytes +
-           static_cast<size_t>(stages) * stage_rows * 128 + kCnStages * v.nt * 4 +
+           static_cast<size_t>(stages) * stage_rows * 128 + norm_bytes +
            static_cast<size_t>(v.ch - 1) * v.sub * kTileM * 8 +
            (kblocks <= 2 ? static_cast<size_t>(4 * v.sub * v.ch) * 4096 : 0) + kMiscBytes;
 }
@@ -794,15 +820,19 @@ cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
 
 cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int *clusters)
 {
+    if (kblocks < 2 || kblocks > 4)
+        return cudaErrorInvalidValue;
     const void *fn = nullptr;
     if (v.ch == 2) {
-        const void *t[4] = {(const void *)assign_pair_kernel<2, 1>, (const void *)assign_pair_kernel<2, 2>,
-                            (const void *)assign_pair_kernel<2, 3>, (const void *)assign_pair_kernel<2, 4>};
-        fn = t[kblocks - 1];
+        const void *t[3] = {(const void *)assign_pair_kernel<2, 2>,
+                            (const void *)assign_pair_kernel<2, 3>,
+                            (const void *)assign_pair_kernel<2, 4>};
+        fn = t[kblocks - 2];
     } else {
-        const void *t[4] = {(const void *)assign_pair_kernel<4, 1>, (const void *)assign_pair_kernel<4, 2>,
-                            (const void *)assign_pair_kernel<4, 3>, (const void *)assign_pair_kernel<4, 4>};
-        fn = t[kblocks - 1];
+        const void *t[3] = {(const void *)assign_pair_kernel<4, 2>,
+                            (const void *)assign_pair_kernel<4, 3>,
+                            (const void *)assign_pair_kernel<4, 4>};
+        fn = t[kblocks - 2];
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);

@@ -19,6 +19,8 @@
 
 #include "kmassign.h"
 
+#include <cuda_bf16.h>
+
 namespace kma {
 namespace {
 
@@ -38,6 +40,15 @@ constexpr int kBarCnFull = kBarCEmpty + kMaxStages;   // [kCnStages]
 constexpr int kBarCnEmpty = kBarCnFull + kCnStages;   // [kCnStages]
 constexpr int kNumBars = kBarCnEmpty + kCnStages;
 constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot + abort flag
+// Norm folding (D <= 64): the norms enter the accumulator through one more
+// K = 16 MMA step per tile, A = a constant tile of ones, B = the tile's
+// -||c||^2 / 2 split into three bf16 parts.  Shared memory: the ones tile,
+// then kFoldStages slots of NT rows x 32 bytes (plain K-major layout: 8-row
+// groups of 256 bytes, each two 128-byte core matrices along K).
+constexpr int kFoldStages = 3;
+constexpr uint32_t kOnesBytes = 4096;                 // 128 rows x 16 columns of bf16 1.0
+constexpr uint32_t kFoldLbo = 128;                    // between the two core matrices along K
+constexpr uint32_t kFoldSbo = 256;                    // between 8-row groups
 constexpr uint32_t kConsumerBarrier = 1;              // named barrier id
 // Bound on the teardown waits after an abort (copies and MMAs in flight
 // always finish; this only guards against a hardware failure).
@@ -154,6 +165,22 @@ __device__ __forceinline__ float chunk_min(const float (&s)[32])
     return min3(b0, b1, min2(b2, b3));
 }
 
+// Maximum of 32 values by a tree of 3-input maxes (a NaN is ignored unless
+// every value is NaN).
+__device__ __forceinline__ float chunk_max(const float (&s)[32])
+{
+    float a[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i)
+        a[i] = max3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+    a[10] = max2(s[30], s[31]);
+    const float b0 = max3(a[0], a[1], a[2]);
+    const float b1 = max3(a[3], a[4], a[5]);
+    const float b2 = max3(a[6], a[7], a[8]);
+    const float b3 = max2(a[9], a[10]);
+    return max3(b0, b1, max2(b2, b3));
+}
+
 // s[i] = fmaf(-2, acc[i], cnorm[j0 + i]) in place, norms from shared memory.
 __device__ __forceinline__ void apply_norms(float (&v)[32], uint32_t cn_addr)
 {
@@ -166,8 +193,9 @@ __device__ __forceinline__ void apply_norms(float (&v)[32], uint32_t cn_addr)
 }
 
 // Barriers of a single-block kernel with kConsumerWarps consumer warps
-// (thread 0 only).
-template <int kConsumerWarps>
+// (thread 0 only).  With FOLD the norm slots are freed by the MMA warp's
+// commit instead of by the consumers.
+template <int kConsumerWarps, bool FOLD = false>
 __device__ __forceinline__ void init_barriers(uint32_t bar_base, volatile uint32_t *abort_flag)
 {
     auto bar = [&](int i) -> uint32_t { return bar_base + 8u * static_cast<uint32_t>(i); };
@@ -186,7 +214,7 @@ __device__ __forceinline__ void init_barriers(uint32_t bar_base, volatile uint32
     }
     for (int s = 0; s < kCnStages; ++s) {
         mbar_init(bar(kBarCnFull + s), 32);
-        mbar_init(bar(kBarCnEmpty + s), kConsumerWarps);
+        mbar_init(bar(kBarCnEmpty + s), FOLD ? 1 : kConsumerWarps);
     }
     *abort_flag = 0u;
     fence_mbar_init();
@@ -279,18 +307,21 @@ __device__ __forceinline__ void x_role(const AssignParams &p, const CUtensorMap 
 // unrolled at compile time with the operand descriptors computed once per
 // unit: the tensor pipe's issue queue is shallow and any extra work between
 // MMAs shows up as pipe bubbles.
-template <int SUB, int NT, int KB>
+// With FOLD, each tile gets one more K = 16 step that adds -||c||^2 / 2
+// (ones x the norm slot the norm warp filled), and its commit frees the slot.
+template <int SUB, int NT, int KB, bool FOLD = false>
 __device__ __forceinline__ void mma_role(const AssignParams &p, uint32_t x_base, uint32_t c_base,
                                          uint32_t bar_base, uint32_t tmem_base,
-                                         volatile uint32_t *abort_flag)
+                                         volatile uint32_t *abort_flag, uint32_t fold_base = 0)
 {
     constexpr uint32_t kCStageBytes = NT * 128;
     constexpr uint32_t kXBufBytes = SUB * KB * kXTileBytes;
     constexpr uint32_t kAccCols = SUB * NT;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, NT);
     auto bar = [&](int i) -> uint32_t { return bar_base + 8u * static_cast<uint32_t>(i); };
-    uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0;
+    uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0, fold_used = 0;
     bool ok = true, issued = false;
+    const uint64_t ones_desc = FOLD ? plain_kmajor_desc(fold_base, kFoldLbo, kFoldSbo) : 0;
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
         const Unit w = decode_unit<SUB>(p, u);
         const uint32_t xb = x_used % p.xbufs;
@@ -338,6 +369,22 @@ __device__ __forceinline__ void mma_role(const AssignParams &p, uint32_t x_base,
             }
             if (!ok)
                 break;
+            if (FOLD) {
+                const uint32_t fb = fold_used % kFoldStages;
+                const uint32_t fph = (fold_used / kFoldStages) & 1u;
+                if (!(ok = wait_warp(bar(kBarCnFull + fb), fph, abort_flag, p.timeout_ns)))
+                    break;
+                const uint64_t bdesc =
+                    plain_kmajor_desc(fold_base + kOnesBytes + fb * NT * 32u, kFoldLbo, kFoldSbo);
+                if (elect_one()) {
+#pragma unroll
+                    for (int t = 0; t < SUB; ++t)
+                        mma_bf16(d_tmem + t * NT, ones_desc, bdesc, kIdesc, 1u);
+                    mma_commit(bar(kBarCnEmpty + fb));
+                }
+                __syncwarp();
+                ++fold_used;
+            }
             if (elect_one())
                 mma_commit(bar(kBarAccFull + as));
             __syncwarp();
@@ -386,6 +433,117 @@ __device__ __forceinline__ void norm_role(const AssignParams &p, float *cn_smem,
             }
             mbar_arrive(bar(kBarCnFull + b));   // release: this lane's stores
         }
+    }
+}
+
+// Fill the ones tile and zero the norm slots (all threads of the block, before
+// the block-wide barrier that follows the set-up).  The second core matrix of
+// every slot row stays zero, so only the first 16 bytes change per tile.
+template <int NT>
+__device__ __forceinline__ void fold_init(uint32_t fold_base)
+{
+    constexpr uint32_t kBytes = kOnesBytes + kFoldStages * NT * 32u;
+    const uint32_t one2 = 0x3F803F80u;   // two bf16 1.0
+    for (uint32_t off = threadIdx.x * 16u; off < kBytes; off += blockDim.x * 16u) {
+        const uint32_t w = off < kOnesBytes ? one2 : 0u;
+        st_shared_v4_u32(fold_base + off, w, w, w, w);
+    }
+    fence_proxy_async_smem();
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float v)
+{
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+}
+
+// Norm warp with FOLD: per tile, -||c_j||^2 / 2 for its NT centroids (NaN
+// past K) split into three bf16 parts h + m + l (each the rounding of what
+// the previous parts leave, so the sum carries the fp32 value's 24 bits), at
+// K positions 0, 1, 2 of the tile's slot.  A non-finite value goes whole
+// into h.  The MMA warp waits on these slots, so the next tile's norms are
+// loaded before this tile's are split and stored (their latency overlaps).
+template <int SUB, int NT>
+__device__ __forceinline__ void fold_norm_role(const AssignParams &p, uint32_t fold_base,
+                                               uint32_t bar_base, volatile uint32_t *abort_flag)
+{
+    constexpr int kPer = NT / 32;   // centroids per lane per tile
+    auto bar = [&](int i) -> uint32_t { return bar_base + 8u * static_cast<uint32_t>(i); };
+    const int lane = threadIdx.x & 31;
+    const float kNaN = __int_as_float(0x7fc00000);
+    auto load = [&](int tile, float (&cn)[kPer]) {
+        const int j = tile * NT;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const int i = e * 32 + lane;
+            cn[e] = (j + i < p.K) ? __ldg(p.cnorm + j + i) : kNaN;
+        }
+    };
+    // The block's tiles in schedule order: (unit u, tile) pairs.
+    int u = blockIdx.x;
+    Unit w{};
+    int tile = 0;
+    bool have = u < p.num_units;
+    if (have) {
+        w = decode_unit<SUB>(p, u);
+        tile = w.t_begin;
+    }
+    float cur[kPer];
+    if (have)
+        load(tile, cur);
+    uint32_t n = 0;
+    while (have) {
+        // next tile of the schedule, and its norms in flight
+        int u2 = u, tile2 = tile + 1;
+        Unit w2 = w;
+        if (tile2 >= w.t_end) {
+            u2 = u + gridDim.x;
+            if (u2 < p.num_units) {
+                w2 = decode_unit<SUB>(p, u2);
+                tile2 = w2.t_begin;
+            }
+        }
+        const bool have2 = u2 < p.num_units;
+        float nxt[kPer];
+        if (have2)
+            load(tile2, nxt);
+        // split this tile's norms
+        uint32_t w0[kPer], w1[kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const float v = -0.5f * cur[e];
+            if (isfinite(v)) {
+                const float h = __bfloat162float(__float2bfloat16_rn(v));
+                const float r = v - h;
+                const float m = __bfloat162float(__float2bfloat16_rn(r));
+                w0[e] = bf16_bits(h) | (bf16_bits(m) << 16);
+                w1[e] = bf16_bits(r - m);
+            } else {
+                w0[e] = bf16_bits(v);
+                w1[e] = 0u;
+            }
+        }
+        const uint32_t b = n % kFoldStages;
+        const uint32_t ph = (n / kFoldStages) & 1u;
+        if (!wait_warp(bar(kBarCnEmpty + b), ph ^ 1u, abort_flag, p.timeout_ns))
+            break;
+        const uint32_t slot = fold_base + kOnesBytes + b * NT * 32u;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const int i = e * 32 + lane;
+            st_shared_v4_u32(slot + static_cast<uint32_t>(i >> 3) * kFoldSbo +
+                                 static_cast<uint32_t>(i & 7) * 16u,
+                             w0[e], w1[e], 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarCnFull + b));   // release: this lane's stores
+        ++n;
+        u = u2;
+        w = w2;
+        tile = tile2;
+        have = have2;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            cur[e] = nxt[e];
     }
 }
 

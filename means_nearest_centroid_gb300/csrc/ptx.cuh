@@ -30,6 +30,13 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Make this thread's generic-proxy shared-memory stores visible to the async
+// proxy (tcgen05.mma operands written by threads, not by TMA).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -114,6 +121,14 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
+}
+
+__device__ __forceinline__ void st_shared_v4_u32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                                 uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d)
@@ -313,6 +328,19 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor, K-major without swizzling: 8-row x
+// 16-byte core matrices, `lbo` bytes between the two core matrices of one
+// K = 16 step (along K), `sbo` bytes between 8-row groups (along M or N).
+__device__ __forceinline__ uint64_t plain_kmajor_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;   // layout type 0 (no swizzle) at [61, 64)
+    return d;
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator [4,6)=1, A bf16
 // [7,10)=1, B bf16 [10,13)=1, both K-major (bits 15,16 = 0), N>>3 at [17,23),
 // M>>4 at [24,29).
@@ -349,6 +377,21 @@ __device__ __forceinline__ float min2(float a, float b)
 {
     float d;
     asm("min.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// Maximum of three; a NaN operand is ignored unless all are NaN.
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float max2(float a, float b)
+{
+    float d;
+    asm("max.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
     return d;
 }
 

@@ -30,6 +30,15 @@ PLANS = [
 ]
 
 
+def is_pair(plan):
+    return plan.get("rows_per_cta") == 256 and plan.get("centroids_per_tile") == 256
+
+
+def plans_for(D):
+    """The plans a shape can run: the CTA-pair kernel exists for D > 64 only."""
+    return [p for p in PLANS if D > 64 or not is_pair(p)]
+
+
 @pytest.fixture(scope="module")
 def dev():
     if not torch.cuda.is_available():
@@ -96,6 +105,10 @@ SHAPES = [(1, 1, 16), (1, 3, 64), (5, 7, 32), (300, 130, 64), (129, 257, 256),
 @pytest.mark.parametrize("pi", range(len(PLANS)))
 def test_float_shapes_all_plans(dev, N, K, D, pi):
     X, C = workloads.blobs(N, K, D, seed=N * 7 + K * 3 + D)
+    if PLANS[pi] not in plans_for(D):
+        with pytest.raises(km.KmassignError, match="KMASSIGN_ERR_ARG"):
+            run(dev, X, C, plan=PLANS[pi])
+        return
     idx, ms = run(dev, X, C, plan=PLANS[pi], with_cnorm=(pi % 2 == 1))
     rep = parity.compare(X, C, idx, ms)
     assert rep.ok(), rep
@@ -105,7 +118,7 @@ def test_float_shapes_all_plans(dev, N, K, D, pi):
 def test_integer_shapes_bit_exact(dev, N, K, D):
     X, C = workloads.integers(N, K, D, seed=N + K + D)
     results = []
-    for plan in PLANS:
+    for plan in plans_for(D):
         idx, ms = run(dev, X, C, plan=plan)
         rep = parity.compare(X, C, idx, ms, integer=True)
         assert rep.ok() and rep.idx_mismatches == 0, (plan, rep)
@@ -117,7 +130,7 @@ def test_integer_shapes_bit_exact(dev, N, K, D):
 
 def test_adversarial_reduced_bit_exact(dev):
     X, C = workloads.adversarial(6000, 2048, 64, seed=44)
-    for plan in PLANS:
+    for plan in plans_for(64):
         idx, ms = run(dev, X, C, plan=plan)
         rep = parity.compare(X, C, idx, ms, integer=True)
         assert rep.ok() and rep.idx_mismatches == 0, (plan, rep)
@@ -126,7 +139,20 @@ def test_adversarial_reduced_bit_exact(dev):
 def test_plans_give_identical_bits_on_float_data(dev):
     X, C = workloads.iid(1500, 1300, 128, seed=99)
     ref = None
-    for plan in PLANS:
+    for plan in plans_for(128):
+        idx, ms = run(dev, X, C, plan=plan)
+        if ref is None:
+            ref = (idx, ms)
+            continue
+        assert torch.equal(idx, ref[0]), plan
+        assert torch.equal(ms.view(torch.int32), ref[1].view(torch.int32)), plan
+
+
+def test_plans_give_identical_bits_on_float_data_with_pairs(dev):
+    """D > 64: the CTA-pair kernel joins the comparison (D = 256 here)."""
+    X, C = workloads.iid(1500, 1300, 256, seed=98)
+    ref = None
+    for plan in plans_for(256):
         idx, ms = run(dev, X, C, plan=plan)
         if ref is None:
             ref = (idx, ms)
