@@ -360,17 +360,38 @@ def assign(X, C, cnorm=None, with_minscore: bool = False, stream=None):
     return (idx, ms) if with_minscore else idx
 
 
+def _slices(N: int, chunks: int, first_rows):
+    """Row boundaries of the X slices: ``first_rows`` for the first (its copy
+    is the only one nothing overlaps; default an even share), then the rest in
+    equal parts."""
+    chunks = max(1, min(int(chunks), max(1, N)))
+    if chunks == 1 or N == 0:
+        return [0, N]
+    if first_rows is None:
+        first_rows = -(-N // chunks)
+    first = max(1, min(int(first_rows), N))
+    rest = N - first
+    per = -(-rest // (chunks - 1)) if rest else 0
+    bounds = [0, first]
+    while bounds[-1] < N:
+        bounds.append(min(N, bounds[-1] + per))
+    return bounds
+
+
 def assign_host(X_host, C_host, idx_host=None, device=None, stream=None, scratch=None,
-                chunks: int = 4):
+                chunks: int = 8, first_rows=None):
     """End-to-end assignment of host tensors (X and C ideally pinned).
 
     C is copied and its norms computed first; X is copied in ``chunks`` row
     slices through two device buffers on a copy stream while the previous
     slice is assigned on the compute stream, and each slice's idx is copied
-    back on a third stream as soon as it is ready.  Every step of the method still runs in the
+    back on a third stream as soon as it is ready.  ``first_rows`` sets the
+    first slice's size (default: even slices; on GB300 a shorter first slice
+    measured no gain, since the kernel itself slows while copies run).  Every
+    step of the method still runs in the
     library's kernels; this only overlaps the host<->device copies with them.
     ``scratch`` may hold preallocated device tensors {"X", "C", "idx"} (X of
-    at least one chunk's rows, C of C_host's shape, idx of N rows).  Returns
+    at least two slices' rows, C of C_host's shape, idx of N rows).  Returns
     ``idx_host`` (pinned int32, allocated if None) after synchronising.
     """
     device = torch.device("cuda") if device is None else torch.device(device)
@@ -380,8 +401,8 @@ def assign_host(X_host, C_host, idx_host=None, device=None, stream=None, scratch
         scratch = {}
     if idx_host is None:
         idx_host = torch.empty(N, dtype=torch.int32, pin_memory=True)
-    chunks = max(1, min(int(chunks), max(1, N)))
-    rows = (N + chunks - 1) // chunks if N else 0
+    bounds = _slices(N, chunks, first_rows)
+    rows = max((b - a for a, b in zip(bounds, bounds[1:])), default=0)
     copy = scratch.get("copy_stream")
     if copy is None:
         copy = torch.cuda.Stream(device)
@@ -404,8 +425,7 @@ def assign_host(X_host, C_host, idx_host=None, device=None, stream=None, scratch
         Cd.copy_(C_host, non_blocking=True)
         kmassign_norms(Cd, out=cn, stream=compute)
     done = [None, None]          # compute finished with buffer slot b
-    for c in range(chunks):
-        b0, b1 = c * rows, min(N, (c + 1) * rows)
+    for c, (b0, b1) in enumerate(zip(bounds, bounds[1:])):
         if b0 >= b1:
             break
         slot = c % 2

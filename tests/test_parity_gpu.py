@@ -199,10 +199,17 @@ def test_assign_host_end_to_end(dev):
     assert rep.ok(), rep
 
 
-@pytest.mark.parametrize("N,chunks", [(3, 4), (1001, 4), (5000, 3), (777, 1)])
+@pytest.mark.parametrize("N,chunks", [(3, 4), (1001, 4), (5000, 3), (777, 1), (6000, 8)])
 def test_assign_host_chunked_matches_device_call(dev, N, chunks):
     X, C = workloads.blobs(N, 300, 64, seed=N)
     got = km.assign_host(X.pin_memory(), C.pin_memory(), chunks=chunks)
+    ref = km.kmassign(X.to(dev), C.to(dev)).cpu()
+    assert torch.equal(got, ref)
+
+
+def test_assign_host_short_first_slice(dev):
+    X, C = workloads.blobs(4000, 300, 64, seed=40)
+    got = km.assign_host(X.pin_memory(), C.pin_memory(), chunks=5, first_rows=37)
     ref = km.kmassign(X.to(dev), C.to(dev)).cpu()
     assert torch.equal(got, ref)
 
