@@ -107,22 +107,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint3
         : "memory");
 }
 
-// Bring a tile of a tensor into L2 ahead of its load (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void *map, int32_t x, int32_t y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
-}
-
 __device__ __forceinline__ void st_shared_v4_u32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                                  uint32_t d)
 {
