@@ -176,10 +176,12 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 // (the five benchmark workloads, every shape forced in turn):
 //   * tensor pipe: a 128x256x16 bf16 MMA takes 128 clocks back to back, a
 //     128x128x16 one ~80 with two accumulators and ~92 with one, plus ~500
-//     clocks of hand-over per tile;
+//     clocks of hand-over per tile (D <= 64: one more MMA per tile, the
+//     folded norms);
 //   * epilogue floor per tile (latency-bound reduction): ~2150 clocks for a
 //     128x256 tile with 8 or 16 warps, ~1700 / ~1550 for a 256x128 tile with
-//     8 / 16 warps, ~1400 for a 128x128 tile with 4 warps;
+//     8 / 16 warps (~1250 / ~1600 with folded norms), ~1400 for a 128x128
+//     tile with 4 warps;
 //   * a unit pays ~5000 clocks to load its X tile and fill the pipe;
 //   * any split pays ~12000 clocks for the key memset, the finalize kernel
 //     and their launches.
@@ -228,9 +230,14 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const int64_t ntiles = cdiv(K, v.nt);
         const int64_t R = cdiv(N, static_cast<int64_t>(rows));
         const double mma_clk = v.nt == 256 ? 128.0 : (v.sub == 2 ? 80.0 : 92.0);
-        const double tile_mma = double(v.sub) * kblocks * 4 * mma_clk + 500.0;
-        const double tile_epi = v.nt == 256 ? 2150.0
-                                : v.sub == 2 ? (v.ch == 2 ? 1550.0 : 1700.0) : 1400.0;
+        // D <= 64 single-block kernels fold the norms into one more MMA step
+        // and their reduction is lighter (256x128 tiles: ~1250 clocks with 8
+        // warps, ~1600 with 16, measured at D = 64).
+        const bool fold = !topk && !v.pair && kblocks == 1;
+        const double tile_mma = double(v.sub) * (kblocks * 4 + (fold ? 1 : 0)) * mma_clk + 500.0;
+        const double tile_epi =
+            fold ? (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1600.0 : 1250.0) : 1400.0)
+                 : (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1550.0 : 1700.0) : 1400.0);
         // The pair kernel couples both SMs' consumers on every tile; measured
         // ~20% slower than the single-block shapes, so it is only chosen when
         // forced (kmassign_ex).
