@@ -9,7 +9,8 @@ Metric: TFLOP/s counted as 2*N*K*D per step (the dense X.C^T the method
 performs), whole job over all ranks.  Three seeded input sets rotate between
 steps (410 MB in total, more than the 126 MB L2), as in the pages' method
 (flashlib PR #22, "Benchmark methodology": three seeded sets rotated between
-calls, warm-up calls, CUDA-event timing).
+calls, warm-up calls, CUDA-event timing).  Workloads whose three sets fit in
+twice the L2 get an L2 flush between timed steps instead (--l2).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload KEY]
   python bench.py --impl reference ...   # the fp64 CPU oracle, same metric
@@ -46,6 +47,7 @@ UNIT = "TFLOP/s"
 # results": N=262,144, D=256, K=16,384 in 1.8615 ms -> 1,181 TFLOP/s).
 PAGES_B200_TFLOPS = {"iid_normal": 2 * 262144 * 16384 * 256 / 1.8615e-3 / 1e12}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+L2_BYTES_FALLBACK = 126 * 1024 * 1024    # GB300, when the device does not report it
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "assign_kernel_traffic.txt")
 
 
@@ -479,6 +481,9 @@ def main():
                     help="comma-separated k values: time the k-nearest call instead")
     ap.add_argument("--distances", action="store_true",
                     help="with --topk: write squared distances instead of scores")
+    ap.add_argument("--l2", default="auto", choices=["auto", "flush", "none"],
+                    help="flush L2 between timed steps: auto = when the rotating inputs do not "
+                         "exceed twice the L2")
     ap.add_argument("--parity-rows", type=int, default=256)
     ap.add_argument("--N", type=int, default=None, help="override the workload's N")
     ap.add_argument("--K", type=int, default=None, help="override the workload's K")
@@ -535,8 +540,21 @@ def main():
         for (X, C), cn in zip(dsets, cns):
             km.kmassign_norms(C, out=cn, stream=stream)
 
-    def step(i, ev_mid=None, ev_end=None):
+    # L2: the three rotating sets together must exceed L2 between timed steps;
+    # when they do not (the small workloads), a buffer larger than L2 is
+    # written between steps, outside the steps' own events.
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0)) or \
+        L2_BYTES_FALLBACK
+    set_bytes = sum(X.numel() * 2 + C.numel() * 2 + N * 4 + K * 4 for X, C in dsets)
+    flush = args.l2 == "flush" or (args.l2 == "auto" and set_bytes < 2 * l2_bytes)
+    flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=device) if flush else None
+
+    def step(i, ev_mid=None, ev_end=None, ev_begin=None):
         X, C = dsets[i % 3]
+        if flush_buf is not None:
+            flush_buf.fill_(i & 0xff)
+        if ev_begin is not None:
+            ev_begin.record(stream)
         if norms_in_step:
             km.kmassign_norms(C, out=cns[i % 3], stream=stream)
         if ev_mid is not None:
@@ -554,6 +572,7 @@ def main():
     if rc != 0:
         raise SystemExit(f"warm-up failed: {km.kmassign_strerror(rc)}")
 
+    begins = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
@@ -564,7 +583,7 @@ def main():
     wall0 = time.time()
     t_start.record(stream)
     for i in range(args.steps):
-        step(i, mids[i], ends[i])
+        step(i, mids[i], ends[i], begins[i])
     t_stop.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -576,6 +595,9 @@ def main():
     sampler.stop()
     total_ms = t_start.elapsed_time(t_stop)
     kern_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+    if flush_buf is not None:
+        # the flushes sit between the steps: count the steps' own time only
+        total_ms = sum(b.elapsed_time(e) for b, e in zip(begins, ends))
     total_ms = max_over_ranks(total_ms, dist, device)
     ms_per_step = total_ms / args.steps
     value = flops * ws * args.steps / (total_ms * 1e-3) / 1e12
@@ -663,8 +685,15 @@ def main():
         "config": {"workload": (f"{key} distribution resized to N={N}, D={D}, K={K}"
                                 if resized else w.text), "key": key, "N": N, "D": D, "K": K,
                    "norms_in_step": norms_in_step,
-                   "l2": "3 rotating seeded input sets per GPU, larger than the 126 MB L2 "
-                         "together",
+                   "l2": (f"L2 ({l2_bytes / 2**20:.0f} MiB) flushed between timed steps by "
+                          f"writing {2 * l2_bytes / 2**20:.0f} MiB outside the steps' events; "
+                          f"3 rotating sets of {set_bytes / 2**20:.0f} MiB in total"
+                          if flush_buf is not None else
+                          f"3 rotating seeded input sets per GPU, {set_bytes / 2**20:.0f} MiB "
+                          f"together, larger than twice the {l2_bytes / 2**20:.0f} MiB L2"
+                          if set_bytes >= 2 * l2_bytes else
+                          f"not flushed (--l2 none): 3 rotating sets of {set_bytes / 2**20:.0f} "
+                          f"MiB may stay in the {l2_bytes / 2**20:.0f} MiB L2"),
                    "plan": plan, "parallelism": f"points sharded, {ws} independent batches"},
         "roofline": roofline,
         "cpu_baseline": cpu,
