@@ -113,27 +113,37 @@ def _check(code: int, where: str):
         raise KmassignError(code, where)
 
 
-def _stream_ptr(stream) -> ctypes.c_void_p:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_ptr(stream, device=None) -> int:
+    """The cudaStream_t to launch on: ``stream``, else the current stream of
+    ``device`` (the tensors' device), else of the current device."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        if _raw_stream is not None:
+            idx = torch.cuda.current_device() if device is None else device.index
+            return _raw_stream(idx)
+        stream = torch.cuda.current_stream(device)
     if isinstance(stream, torch.cuda.Stream):
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
 def _ptr(t):
-    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _need_cuda(t, name, dtype):
+    # the common case in one expression; the detail only on failure
+    if isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dtype and t.is_contiguous():
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+    raise ValueError(f"{name} must be contiguous")
 
 
 def kmassign_norms(C: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
@@ -143,7 +153,7 @@ def kmassign_norms(C: torch.Tensor, out: torch.Tensor | None = None, stream=None
     if out is None:
         out = torch.empty(K, dtype=torch.float32, device=C.device)
     _need_cuda(out, "out", torch.float32)
-    _check(library().kmassign_norms(_ptr(C), K, D, _ptr(out), _stream_ptr(stream)),
+    _check(library().kmassign_norms(_ptr(C), K, D, _ptr(out), _stream_ptr(stream, C.device)),
            "kmassign_norms")
     return out
 
@@ -167,7 +177,7 @@ def kmassign_ex(X, C, cnorm=None, idx=None, minscore=None, ksplit: int = 0,
         _need_cuda(minscore, "minscore", torch.float32)
     rc = library().kmassign_ex(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, _ptr(idx), _ptr(minscore),
                                int(ksplit), int(rows_per_cta), int(centroids_per_tile),
-                               int(consumer_warps), _stream_ptr(stream))
+                               int(consumer_warps), _stream_ptr(stream, X.device))
     _check(rc, "kmassign_ex")
     return idx
 
@@ -188,7 +198,7 @@ def kmassign(X, C, cnorm=None, idx=None, minscore=None, stream=None):
     if minscore is not None:
         _need_cuda(minscore, "minscore", torch.float32)
     rc = library().kmassign(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, _ptr(idx), _ptr(minscore),
-                            _stream_ptr(stream))
+                            _stream_ptr(stream, X.device))
     _check(rc, "kmassign")
     return idx
 
@@ -215,7 +225,7 @@ def kmassign_noalloc(X, C, cnorm=None, idx=None, minscore=None, stream=None):
     if minscore is not None:
         _need_cuda(minscore, "minscore", torch.float32)
     rc = library().kmassign_noalloc(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, _ptr(idx),
-                                    _ptr(minscore), _stream_ptr(stream))
+                                    _ptr(minscore), _stream_ptr(stream, X.device))
     _check(rc, "kmassign_noalloc")
     return idx
 
@@ -250,10 +260,10 @@ def kmassign_topk(X, C, k: int, cnorm=None, idx=None, score=None, distances: boo
     if ksplit:
         rc = lib.kmassign_topk_ex(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, k, _ptr(idx),
                                   _ptr(score), int(bool(distances)), int(ksplit),
-                                  _stream_ptr(stream))
+                                  _stream_ptr(stream, X.device))
     else:
         rc = lib.kmassign_topk(_ptr(X), _ptr(C), _ptr(cnorm), N, K, D, k, _ptr(idx), _ptr(score),
-                               int(bool(distances)), _stream_ptr(stream))
+                               int(bool(distances)), _stream_ptr(stream, X.device))
     _check(rc, "kmassign_topk")
     return idx, score
 
@@ -286,7 +296,8 @@ def kmassign_update(X, idx, K: int, sums=None, counts=None, method: int = 0, str
     _need_cuda(sums, "sums", torch.float32)
     _need_cuda(counts, "counts", torch.int32)
     _check(library().kmassign_update_ex(_ptr(X), _ptr(idx), N, int(K), D, _ptr(sums),
-                                        _ptr(counts), int(method), _stream_ptr(stream)),
+                                        _ptr(counts), int(method),
+                                        _stream_ptr(stream, X.device)),
            "kmassign_update")
     return sums, counts
 
@@ -303,7 +314,8 @@ def kmassign_centroids(sums, counts, C_old, C_new=None, means=None, stream=None)
     if means is not None:
         _need_cuda(means, "means", torch.float32)
     _check(library().kmassign_centroids(_ptr(sums), _ptr(counts), _ptr(C_old), K, D, _ptr(C_new),
-                                        _ptr(means), _stream_ptr(stream)), "kmassign_centroids")
+                                        _ptr(means), _stream_ptr(stream, sums.device)),
+           "kmassign_centroids")
     return C_new
 
 
@@ -320,7 +332,7 @@ def kmassign_lloyd(X, C, iters: int, idx=None, stream=None):
         idx = torch.empty(N, dtype=torch.int32, device=X.device)
     _need_cuda(idx, "idx", torch.int32)
     _check(library().kmassign_lloyd(_ptr(X), _ptr(C), N, K, D, int(iters), _ptr(idx),
-                                    _stream_ptr(stream)), "kmassign_lloyd")
+                                    _stream_ptr(stream, X.device)), "kmassign_lloyd")
     return idx
 
 
