@@ -77,6 +77,18 @@ def test_update_skewed_clusters(dev, method):
     check_sums(Xi, idx, K, sums, counts, integer=True)
 
 
+@pytest.mark.parametrize("N,K,D", [(400_000, 1000, 64), (300_000, 2000, 16), (2_000_000, 500, 32)])
+def test_update_sorted_many_points_per_centroid(dev, N, K, D):
+    """N >> K: the sort counts in shared memory per block first."""
+    Xi, _ = workloads.integers(N, 1, D, seed=K)
+    g = np.random.default_rng(K)
+    idx = g.integers(-1, K + 1, N).astype(np.int32)
+    sums, counts = km.kmassign_update(Xi.to(dev), torch.from_numpy(idx).to(dev), K, method=2)
+    check_sums(Xi, idx, K, sums, counts, integer=True)
+    a = km.kmassign_update(Xi.to(dev), torch.from_numpy(idx).to(dev), K, method=1)
+    assert torch.equal(a[0], sums) and torch.equal(a[1], counts)
+
+
 def test_update_methods_agree_on_integers(dev):
     X, _ = workloads.integers(30000, 1, 128, seed=6)
     idx = torch.from_numpy(np.random.default_rng(6).integers(0, 900, 30000).astype(np.int32))
