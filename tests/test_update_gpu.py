@@ -53,9 +53,12 @@ METHODS = [0, 1, 2]   # automatic, atomic, sorted
 
 @pytest.mark.parametrize("N,K,D", [(1, 1, 16), (1000, 37, 64), (5000, 300, 128), (3000, 17, 256),
                                    (2048, 1000, 48), (999, 5, 80), (20000, 5000, 96),
-                                   (9000, 70000, 16)])
+                                   (9000, 70000, 16), (40000, 40000, 32), (300000, 16385, 16),
+                                   (70000, 65536, 16)])
 @pytest.mark.parametrize("method", METHODS)
 def test_update_float_and_integer(dev, N, K, D, method):
+    """Ragged shapes; K past one scan tile of 16,384 bins, at the one-block
+    limit 65,536 and past it (the multi-block scan)."""
     X, C = workloads.blobs(N, min(K, 4096), D, seed=N + D)
     g = np.random.default_rng(N)
     idx = g.integers(-2, K + 2, N).astype(np.int32)          # includes ids to skip
