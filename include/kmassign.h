@@ -127,6 +127,14 @@ int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int
 int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9);
 
 /*
+ * The plan kmassign_ex would run with the same forcing arguments (same
+ * meaning and errors as there; 0 leaves a field to the planner), in
+ * kmassign_plan's layout.  Launches nothing.
+ */
+int kmassign_plan_ex(int64_t N, int64_t K, int64_t D, int ksplit, int rows_per_cta,
+                     int centroids_per_tile, int consumer_warps, int32_t *out9);
+
+/*
  * Synchronise `stream`, then report and clear the device status word:
  * KMASSIGN_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
  * check, KMASSIGN_ERR_CUDA if the stream reports an error, else KMASSIGN_OK.

@@ -69,6 +69,8 @@ def _declare(lib):
     lib.kmassign_noalloc.restype = i32
     lib.kmassign_plan.argtypes = [i64, i64, i64, vp]
     lib.kmassign_plan.restype = i32
+    lib.kmassign_plan_ex.argtypes = [i64, i64, i64, i32, i32, i32, i32, vp]
+    lib.kmassign_plan_ex.restype = i32
     lib.kmassign_update.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
     lib.kmassign_update.restype = i32
     lib.kmassign_update_ex.argtypes = [vp, vp, i64, i64, i64, vp, vp, i32, vp]
@@ -268,9 +270,13 @@ def kmassign_topk(X, C, k: int, cnorm=None, idx=None, score=None, distances: boo
     return idx, score
 
 
-def kmassign_plan(N: int, K: int, D: int) -> dict:
+def kmassign_plan(N: int, K: int, D: int, ksplit: int = 0, rows_per_cta: int = 0,
+                  centroids_per_tile: int = 0, consumer_warps: int = 0) -> dict:
+    """The plan kmassign (or, with forcing arguments, kmassign_ex) would run."""
     out = (ctypes.c_int32 * 9)()
-    _check(library().kmassign_plan(int(N), int(K), int(D), ctypes.cast(out, ctypes.c_void_p)),
+    _check(library().kmassign_plan_ex(int(N), int(K), int(D), int(ksplit), int(rows_per_cta),
+                                      int(centroids_per_tile), int(consumer_warps),
+                                      ctypes.cast(out, ctypes.c_void_p)),
            "kmassign_plan")
     keys = ["ksplit", "rows_per_cta", "centroids_per_tile", "grid", "stages", "xbufs",
             "whole_row_tiles", "split_row_tiles", "consumer_warps"]

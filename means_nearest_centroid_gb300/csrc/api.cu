@@ -238,10 +238,15 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const double tile_epi =
             fold ? (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1600.0 : 1250.0) : 1400.0)
                  : (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1550.0 : 1700.0) : 1400.0);
-        // The pair kernel couples both SMs' consumers on every tile; measured
-        // ~20% slower than the single-block shapes, so it is only chosen when
-        // forced (kmassign_ex).
-        const double tile = std::max(tile_mma, tile_epi) * (v.pair ? 1.25 : 1.0);
+        // The pair kernel halves each SM's C traffic but couples both SMs'
+        // consumers on every tile.  Measured against the single-block shapes
+        // (iid inputs, medians of 30 calls): 5-8% faster at D = 192 and at
+        // D = 256 with at most 16 tiles per unit; at D = 256 with 64 tiles
+        // per unit its time varies by +-4% between runs and averages level;
+        // at D = 128 it is 3-9% slower.
+        const double pair_factor =
+            (kblocks == 3 || (kblocks == 4 && ntiles <= 16)) ? 0.94 : 1.10;
+        const double tile = std::max(tile_mma, tile_epi) * (v.pair ? pair_factor : 1.0);
         const double unit_over = 5000.0;
 
         // Candidate (F whole row tiles, split the rest into ks ranges).
@@ -905,19 +910,25 @@ int kmassign_topk_ex(const void *X, const void *C, const float *cnorm, int64_t N
                     static_cast<cudaStream_t>(stream));
 }
 
-int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9)
+int kmassign_plan_ex(int64_t N, int64_t K, int64_t D, int ksplit, int rows_per_cta,
+                     int centroids_per_tile, int consumer_warps, int32_t *out9)
 {
     if (out9 == nullptr)
         return KMASSIGN_ERR_NULL;
     int rc = check_shape(N, K, D);
     if (rc != KMASSIGN_OK)
         return rc;
+    if (ksplit == -1 || (rows_per_cta != 0 && rows_per_cta != 128 && rows_per_cta != 256) ||
+        (centroids_per_tile != 0 && centroids_per_tile != 128 && centroids_per_tile != 256) ||
+        (consumer_warps != 0 && consumer_warps != 4 && consumer_warps != 8 &&
+         consumer_warps != 16))
+        return KMASSIGN_ERR_ARG;
     DeviceInfo dev;
     if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
     Plan plan;
-    if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, 0, 0, 0, 0, false, &plan)) !=
-        KMASSIGN_OK)
+    if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, ksplit, rows_per_cta,
+                        centroids_per_tile, consumer_warps, false, &plan)) != KMASSIGN_OK)
         return rc;
     out9[0] = plan.ksplit;
     out9[1] = (plan.v.pair ? 2 : plan.v.sub) * kma::kTileM;
@@ -929,6 +940,11 @@ int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9)
     out9[7] = plan.rowtiles - plan.split_row0;
     out9[8] = 4 * plan.v.sub * plan.v.ch;
     return KMASSIGN_OK;
+}
+
+int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9)
+{
+    return kmassign_plan_ex(N, K, D, 0, 0, 0, 0, out9);
 }
 
 int kmassign_set_wait_timeout(uint64_t ns)

@@ -351,7 +351,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     constexpr int kMmaWarp = kConsumerWarps + 1;
     constexpr int kNormWarp = kConsumerWarps + 2;
     constexpr int kXWarp = kConsumerWarps + 3;
-    constexpr bool kSnap = KB <= 2;
+    // The pair's half-size C stages leave room for the deferred first-index
+    // search up to D = 192, where its consumers, not the tensor pipe, set the
+    // pace (measured 5-8% faster there; at D = 256 the stages it costs matter
+    // more).
+    constexpr bool kSnap = KB <= 3;
     constexpr int kCW = NT / CH;
     constexpr int kChunks = kCW / 32;
     constexpr int kGroup = kChunks < 4 ? kChunks : 4;
@@ -803,7 +807,9 @@ size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
     return 1024 + static_cast<size_t>(xbufs) * v.sub * kblocks * kXTileBytes +
            static_cast<size_t>(stages) * stage_rows * 128 + norm_bytes +
            static_cast<size_t>(v.ch - 1) * v.sub * kTileM * 8 +
-           (kblocks <= 2 ? static_cast<size_t>(4 * v.sub * v.ch) * 4096 : 0) + kMiscBytes;
+           (kblocks <= 2 || (v.pair && kblocks <= 3) ? static_cast<size_t>(4 * v.sub * v.ch) * 4096
+                                                      : 0) +
+           kMiscBytes;
 }
 
 cudaError_t assign_prepare(const Variant &v, int kblocks, size_t smem)

@@ -133,6 +133,16 @@ def test_topk_argument_errors(lib):
 
 def test_plan_rejects_null_output(lib):
     assert lib.kmassign_plan(10, 5, 64, NULL) == km.STATUS["KMASSIGN_ERR_NULL"]
+    assert lib.kmassign_plan_ex(10, 5, 64, 0, 0, 0, 0, NULL) == km.STATUS["KMASSIGN_ERR_NULL"]
+
+
+def test_plan_ex_rejects_forcing_arguments_no_kernel_has(lib):
+    """Checked before the device is queried, as kmassign_ex checks them."""
+    out = (ctypes.c_int32 * 9)()
+    o = ctypes.cast(out, ctypes.c_void_p)
+    for ks, rows, nt, cw in [(-1, 0, 0, 0), (0, 64, 0, 0), (0, 0, 512, 0), (0, 0, 0, 12)]:
+        assert lib.kmassign_plan_ex(10, 5, 64, ks, rows, nt, cw, o) == km.STATUS["KMASSIGN_ERR_ARG"]
+    assert lib.kmassign_plan_ex(10, 5, 40, 0, 0, 0, 0, o) == km.STATUS["KMASSIGN_ERR_UNSUPPORTED_D"]
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
