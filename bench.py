@@ -610,13 +610,18 @@ def main():
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sha = kernel_source_sha()
     traffic, traffic_rec = load_traffic(sha)
+    pair = plan["rows_per_cta"] == 256 and plan["centroids_per_tile"] == 256
+    tile = f'{plan["rows_per_cta"]}x{plan["centroids_per_tile"]}{" pair" if pair else ""}'
     traffic_bytes = None
-    if traffic is not None and traffic.get("workload") == key:
+    if (traffic is not None and not resized and traffic.get("workload") == key
+            and traffic.get("tile") == tile):
         traffic_bytes = traffic.get("bytes_per_launch")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic_bytes,
                 "peak_source": f"{peak_src} bf16 dense (burst)",
-                "kernel": "assign_kernel (tcgen05)", "kernel_ms_avg": kernel_avg_ms,
+                "kernel": ("assign_pair_kernel (tcgen05.cta_group::2, " if pair
+                           else "assign_kernel (tcgen05, ") + tile + " tiles)",
+                "kernel_ms_avg": kernel_avg_ms,
                 "kernel_ms_median": kernel_med_ms,
                 "algorithmic_bytes": N * D * 2 + K * D * 2 + N * 4 + K * 4}
 

@@ -240,12 +240,11 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
                  : (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1550.0 : 1700.0) : 1400.0);
         // The pair kernel halves each SM's C traffic but couples both SMs'
         // consumers on every tile.  Measured against the single-block shapes
-        // (iid inputs, medians of 30 calls): 5-8% faster at D = 192 and at
-        // D = 256 with at most 16 tiles per unit; at D = 256 with 64 tiles
-        // per unit its time varies by +-4% between runs and averages level;
-        // at D = 128 it is 3-9% slower.
-        const double pair_factor =
-            (kblocks == 3 || (kblocks == 4 && ntiles <= 16)) ? 0.94 : 1.10;
+        // (iid inputs): 5-8% faster at D = 192 and at D = 256 with at most 16
+        // tiles per unit; at D = 256 with 64 tiles per unit level in short
+        // bursts at full clock and 5-7% faster in long runs under the power
+        // cap (less L2 traffic per flop); at D = 128 3-9% slower.
+        const double pair_factor = kblocks >= 3 ? 0.94 : 1.10;
         const double tile = std::max(tile_mma, tile_epi) * (v.pair ? pair_factor : 1.0);
         const double unit_over = 5000.0;
 
