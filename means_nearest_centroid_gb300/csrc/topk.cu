@@ -69,24 +69,12 @@ __device__ __forceinline__ float finish_score(uint32_t o, float xn, bool distanc
     return d < 0.0f ? 0.0f : d;
 }
 
-// s[e] for a run-time e in [0, 32) by a tree of selects (no local memory).
-__device__ __forceinline__ float pick(const float (&s)[32], int e)
+// One 32-bit shared-memory load.
+__device__ __forceinline__ float lds_f32(uint32_t addr)
 {
-    float a[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        a[i] = (e & 1) ? s[2 * i + 1] : s[2 * i];
-    float b[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        b[i] = (e & 2) ? a[2 * i + 1] : a[2 * i];
-    float c[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        c[i] = (e & 4) ? b[2 * i + 1] : b[2 * i];
-    const float d0 = (e & 8) ? c[1] : c[0];
-    const float d1 = (e & 8) ? c[3] : c[2];
-    return (e & 16) ? d1 : d0;
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // A sorted list (ascending by ordered score, then index) of the best L
@@ -159,9 +147,12 @@ struct TopList {
 // enter (a NaN column's index is larger than every NaN held), so a chunk with
 // no number (m is NaN) returns at once: a point whose scores are all NaN
 // costs two comparisons per chunk.
+// The chunk is first copied to this thread's shared slot (float4 i at
+// slot + 512 i, conflict-free across the warp), so each marked column is one
+// shared load instead of a 31-select tree.
 template <int L>
 __device__ __forceinline__ void admit_chunk(TopList<L> &lst, const float (&s)[32], float m,
-                                            int j0, float &thr)
+                                            int j0, float &thr, uint32_t slot)
 {
     if (m != m && lst.o[L - 1] == kNaNOrd)
         return;
@@ -169,10 +160,14 @@ __device__ __forceinline__ void admit_chunk(TopList<L> &lst, const float (&s)[32
 #pragma unroll
     for (int e = 0; e < 32; ++e)
         mask |= (s[e] >= thr) ? 0u : (1u << e);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        st_shared_v4(slot + 512u * i, s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
     while (mask != 0u) {
         const int e = __ffs(mask) - 1;
         mask &= mask - 1u;
-        const uint32_t u = ord_of(pick(s, e));
+        const uint32_t u =
+            ord_of(lds_f32(slot + 512u * static_cast<uint32_t>(e >> 2) + 4u * (e & 3)));
         if (u < lst.o[L - 1])
             lst.push_later(u, j0 + e);
     }
@@ -209,7 +204,8 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
     const uint32_t x_base = base;
     const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
     const uint32_t cn_base = c_base + p.stages * kCStageBytes;   // float[kCnStages][NT]
-    const uint32_t bar_base = cn_base + kCnStages * NT * 4;
+    const uint32_t snap_base = cn_base + kCnStages * NT * 4;   // [warp][8][32] float4
+    const uint32_t bar_base = snap_base + kConsumerWarps * 4096u;
     uint8_t *const sbase = smem_raw + (base - raw);
     uint8_t *misc_ptr = smem_raw + (bar_base - raw) + kNumBars * 8;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(misc_ptr);
@@ -245,6 +241,7 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
         const int q = warp & 3;
         const int t = warp >> 2;
         const bool distances = p.xnorm != nullptr;
+        const uint32_t slot = snap_base + 4096u * warp + 16u * lane;
         uint32_t acc_used = 0;
         bool ok = true;
 
@@ -292,7 +289,7 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c)
                             if (!(m[c] >= thr))
-                                admit_chunk<L>(lst, v[c], m[c], jg + 32 * c, thr);
+                                admit_chunk<L>(lst, v[c], m[c], jg + 32 * c, thr, slot);
                     }
                     __syncwarp();
                     if (lane == 0)
@@ -469,7 +466,8 @@ int topk_list_size(int k)
 size_t topk_smem_bytes(int kblocks, int stages, int xbufs)
 {
     return 1024 + static_cast<size_t>(xbufs) * kTopSub * kblocks * kXTileBytes +
-           static_cast<size_t>(stages) * kTopNt * 128 + kCnStages * kTopNt * 4 + kMiscBytes;
+           static_cast<size_t>(stages) * kTopNt * 128 + kCnStages * kTopNt * 4 +
+           static_cast<size_t>(kTopConsumerWarps) * 4096 + kMiscBytes;
 }
 
 cudaError_t topk_prepare(int kblocks, int list, size_t smem)
