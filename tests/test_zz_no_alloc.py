@@ -28,6 +28,7 @@ CASES = [
     (3000, 5000, 128, False, workloads.blobs),
     (1000, 4096, 256, True, workloads.integers),
     (70000, 3000, 64, False, workloads.blobs),
+    (20000, 8192, 192, False, workloads.blobs),   # CTA-pair plan, tail split
 ]
 
 
