@@ -665,7 +665,7 @@ def main():
                "h2d_bytes_per_step": Xh.numel() * 2 + Ch.numel() * 2,
                "d2h_bytes_per_step": idx_h.numel() * 4, "steps": args.e2e_steps,
                "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
-               "note": "every step: pinned host X and C copied in (X in 8 row slices overlapped "
+               "note": "every step: pinned host X and C copied in (X in row slices of whole waves overlapped "
                        "with the assignment of the previous slice), norms + assignment, idx "
                        "copied out, streams synchronised"}
 

@@ -378,22 +378,41 @@ def assign(X, C, cnorm=None, with_minscore: bool = False, stream=None):
     return (idx, ms) if with_minscore else idx
 
 
-def _slices(N: int, chunks: int, first_rows):
+def _slices(N: int, chunks: int, first_rows, align: int = 1):
     """Row boundaries of the X slices: ``first_rows`` for the first (its copy
     is the only one nothing overlaps; default an even share), then the rest in
-    equal parts."""
+    equal parts.  With ``align`` > 1 (the rows one wave of the assignment's
+    work units covers) the even share is rounded to a whole number of waves,
+    so that no slice but the last ends in a partly filled wave; the last slice
+    takes what remains."""
     chunks = max(1, min(int(chunks), max(1, N)))
     if chunks == 1 or N == 0:
         return [0, N]
+    align = max(1, int(align))
+    share = -(-N // chunks)
+    if align > 1:
+        share = max(align, int(round(share / align)) * align)
     if first_rows is None:
-        first_rows = -(-N // chunks)
+        first_rows = share
     first = max(1, min(int(first_rows), N))
     rest = N - first
-    per = -(-rest // (chunks - 1)) if rest else 0
+    if align > 1:
+        per = share
+    else:
+        per = -(-rest // (chunks - 1)) if rest else 0
     bounds = [0, first]
     while bounds[-1] < N:
         bounds.append(min(N, bounds[-1] + per))
     return bounds
+
+
+def _wave_rows(N: int, K: int, D: int) -> int:
+    """Rows one full wave of the assignment's work units covers for this
+    shape (blocks in flight times rows per block; a CTA pair counts once)."""
+    p = kmassign_plan(max(N, 1), K, D)
+    pair = p["rows_per_cta"] == 256 and p["centroids_per_tile"] == 256
+    units = p["grid"] // 2 if pair else p["grid"]
+    return max(1, units * p["rows_per_cta"])
 
 
 def assign_host(X_host, C_host, idx_host=None, device=None, stream=None, scratch=None,
@@ -419,7 +438,7 @@ def assign_host(X_host, C_host, idx_host=None, device=None, stream=None, scratch
         scratch = {}
     if idx_host is None:
         idx_host = torch.empty(N, dtype=torch.int32, pin_memory=True)
-    bounds = _slices(N, chunks, first_rows)
+    bounds = _slices(N, chunks, first_rows, _wave_rows(N, C_host.shape[0], D) if N else 1)
     rows = max((b - a for a, b in zip(bounds, bounds[1:])), default=0)
     copy = scratch.get("copy_stream")
     if copy is None:
