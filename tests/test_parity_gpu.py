@@ -98,7 +98,9 @@ def test_golden_cases(dev, plan):
 
 # ---------------------------------------------------------------- small shapes
 SHAPES = [(1, 1, 16), (1, 3, 64), (5, 7, 32), (300, 130, 64), (129, 257, 256),
-          (1000, 777, 128), (2000, 1000, 48), (4096, 128, 64), (333, 2049, 96)]
+          (1000, 777, 128), (2000, 1000, 48), (4096, 128, 64), (333, 2049, 96),
+          # D = 192 (CTA pairs by default), K past 65,536, ragged tails
+          (97, 70001, 192), (513, 3001, 192), (260, 4100, 256)]
 
 
 @pytest.mark.parametrize("N,K,D", SHAPES)
