@@ -19,7 +19,7 @@ SPLITS = [0, 2, 3, 5, -2, -3]
 # (N, K, D, k): ragged N and K, every list size (4, 8, 16, 32), k == K
 SHAPES = [(1, 1, 16, 1), (1, 3, 64, 3), (5, 7, 32, 4), (300, 130, 64, 8), (129, 257, 256, 16),
           (1000, 777, 128, 32), (2000, 1000, 48, 5), (333, 2049, 96, 10), (600, 32, 64, 32),
-          (4100, 300, 16, 2)]
+          (4100, 300, 16, 2), (300, 2049, 192, 8)]
 
 
 @pytest.fixture(scope="module")
