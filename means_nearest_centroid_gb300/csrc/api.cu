@@ -110,6 +110,23 @@ bool encode_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t D, uint
     return r == CUDA_SUCCESS;
 }
 
+// The CTA pair's fold operand (fold_operand_blocks(K) blocks of 4 KiB) as
+// rows of 8 bf16 (16 bytes), boxes of 256 rows = one block, no swizzle.
+bool encode_fold_map(CUtensorMap *m, const void *ptr, int64_t K)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    cuuint64_t dims[2] = {8, static_cast<cuuint64_t>(kma::fold_operand_blocks(K)) * 256};
+    cuuint64_t strides[1] = {16};
+    cuuint32_t box[2] = {8, 256};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, uintptr_t a)
 {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
@@ -230,22 +247,34 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const int64_t ntiles = cdiv(K, v.nt);
         const int64_t R = cdiv(N, static_cast<int64_t>(rows));
         const double mma_clk = v.nt == 256 ? 128.0 : (v.sub == 2 ? 80.0 : 92.0);
-        // D <= 64 single-block kernels fold the norms into one more MMA step
-        // and their reduction is lighter (256x128 tiles: ~1250 clocks with 8
-        // warps, ~1600 with 16, measured at D = 64).
-        const bool fold = !topk && !v.pair && kblocks == 1;
+        // Kernels that fold the norms into one more MMA step (single-block
+        // at D <= 64, CTA pairs at D <= 128) have a lighter reduction
+        // (256x128 tiles: ~1250 clocks with 8 warps, ~1600 with 16, measured
+        // at D = 64; a CTA pair's 128x256 per SM: ~1450 with 8 warps,
+        // measured at D = 128 against 1,780 for the 256x128 single block).
+        const bool fold = !topk && kma::assign_folds(v, kblocks);
         const double tile_mma = double(v.sub) * (kblocks * 4 + (fold ? 1 : 0)) * mma_clk + 500.0;
         const double tile_epi =
-            fold ? (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1600.0 : 1250.0) : 1400.0)
-                 : (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1550.0 : 1700.0) : 1400.0);
+            (v.pair && fold)
+                ? (v.ch == 2 ? 1450.0 : 1600.0)
+                : fold ? (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1600.0 : 1250.0) : 1400.0)
+                       : (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1550.0 : 1700.0)
+                                                            : 1400.0);
         // The pair kernel halves each SM's C traffic but couples both SMs'
         // consumers on every tile.  Measured against the single-block shapes
         // (iid inputs): 5-8% faster at D = 192 and at D = 256 with at most 16
         // tiles per unit; at D = 256 with 64 tiles per unit level in short
         // bursts at full clock and 5-7% faster in long runs under the power
-        // cap (less L2 traffic per flop); at D = 128 3-9% slower.
-        const double pair_factor = kblocks >= 3 ? 0.94 : 1.10;
-        const double tile = std::max(tile_mma, tile_epi) * (v.pair ? pair_factor : 1.0);
+        // cap (less L2 traffic per flop).  At D <= 128 it folds, modelled
+        // by its reduction floor above.
+        const double pair_factor = kblocks >= 3 ? 0.94 : 1.0;
+        // A folding pair's tile measured ~1,420 clocks (8 warps) at D = 128,
+        // below its modelled MMA time; its fold operand costs one small
+        // kernel per call.
+        const bool pair_fold = v.pair && fold;
+        const double tile = pair_fold ? (v.ch == 2 ? 1420.0 : 1600.0)
+                                      : std::max(tile_mma, tile_epi) * (v.pair ? pair_factor : 1.0);
+        const double call_over = pair_fold ? 6000.0 : 0.0;
         const double unit_over = 5000.0;
 
         // Candidate (F whole row tiles, split the rest into ks ranges).
@@ -273,7 +302,7 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
                                  double(ns) * (double(chunk) * tile + unit_over);
                 worst = std::max(worst, c);
             }
-            const double cost = worst + (any_split ? 12000.0 : 0.0);
+            const double cost = worst + (any_split ? 12000.0 : 0.0) + call_over;
             if (!found || cost < best_cost * 0.995) {
                 found = true;
                 best_cost = cost;
@@ -452,10 +481,22 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
             cudaMemsetAsync(keys, 0xff, static_cast<size_t>(n_split) * 8, stream) != cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
     }
+    // A CTA pair that folds the norms reads them as a fold operand.
+    void *fold = nullptr;
+    CUtensorMap fmap{};
+    const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
+    if (rc == KMASSIGN_OK && plan.v.pair && kma::assign_folds(plan.v, kblocks)) {
+        if (cudaMallocFromPoolAsync(&fold,
+                                    kma::fold_operand_bytes(K), dev.pool, stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
+        else if (kma::launch_fold_operand(cnorm, K, fold, stream) != cudaSuccess ||
+                 !encode_fold_map(&fmap, fold, K))
+            rc = KMASSIGN_ERR_CUDA;
+    }
     if (rc == KMASSIGN_OK) {
         const AssignParams p = make_params(plan, cnorm, idx, minscore, keys, N, K, D);
-        if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, plan.grid, plan.smem, stream) !=
-            cudaSuccess)
+        if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, fmap, plan.grid, plan.smem,
+                               stream) != cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
         else if (keys != nullptr &&
                  kma::launch_finalize(keys, n_split, idx + row_split,
@@ -463,6 +504,8 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
                                       stream) != cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
     }
+    if (fold != nullptr && cudaFreeAsync(fold, stream) != cudaSuccess)
+        rc = KMASSIGN_ERR_CUDA;
     if (keys != nullptr && cudaFreeAsync(keys, stream) != cudaSuccess)
         rc = KMASSIGN_ERR_CUDA;
     if (tmp_norm != nullptr && cudaFreeAsync(tmp_norm, stream) != cudaSuccess)
@@ -809,9 +852,16 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
     Plan plan;
     if ((rc = make_plan(N, K, D, dev, 0, 0, 0, 0, false, &plan)) != KMASSIGN_OK)
         return rc;
+    // A CTA pair that folds needs a fold operand this entry point has no room
+    // for: take the 256-row single-block shape instead.
+    const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
+    const bool no_pair = plan.v.pair && kma::assign_folds(plan.v, kblocks);
+    const int rows = no_pair ? 256 : 0, nt = no_pair ? 128 : 0;
+    if (no_pair && (rc = make_plan(N, K, D, dev, 0, rows, nt, 0, false, &plan)) != KMASSIGN_OK)
+        return rc;
     // Keys for more points than the array holds: plan without a split.
     if (plan.ksplit > 1 && N - split_first_row(plan) > kNoAllocKeyMax &&
-        (rc = make_plan(N, K, D, dev, 1, 0, 0, 0, false, &plan)) != KMASSIGN_OK)
+        (rc = make_plan(N, K, D, dev, 1, rows, nt, 0, false, &plan)) != KMASSIGN_OK)
         return rc;
 
     CUtensorMap xmap, cmap;
@@ -840,8 +890,9 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
             return KMASSIGN_ERR_CUDA;
     }
     const AssignParams p = make_params(plan, cnorm, idx, minscore, keys, N, K, D);
-    if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, plan.grid, plan.smem, stream) !=
-        cudaSuccess)
+    const CUtensorMap no_fold{};
+    if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, no_fold, plan.grid, plan.smem,
+                           stream) != cudaSuccess)
         return KMASSIGN_ERR_CUDA;
     if (keys != nullptr &&
         kma::launch_finalize(keys, n_split, idx + row_split,

@@ -342,7 +342,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
 template <int CH, int KB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1)
     assign_pair_kernel(const __grid_constant__ CUtensorMap xmap,
-                       const __grid_constant__ CUtensorMap cmap, const AssignParams p)
+                       const __grid_constant__ CUtensorMap cmap,
+                       const __grid_constant__ CUtensorMap fmap, const AssignParams p)
 {
     constexpr int NT = 256;                            // centroids per pair tile
     constexpr int kHalf = 128;                         // C rows each CTA loads
@@ -356,6 +357,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     // pace (measured 5-8% faster there; at D = 256 the stages it costs matter
     // more).
     constexpr bool kSnap = KB <= 3;
+    // D <= 128: the norms enter the accumulator through one more pair MMA
+    // step, A = each CTA's tile of ones, B = each CTA's half of the tile's
+    // fold operand (the split -||c||^2 / 2, precomputed in global memory and
+    // brought in by TMA like a C k-block, so the copy engine, not a thread's
+    // stores, signals the leader).  The consumers then take the largest
+    // t = -s / 2.  Here the pair's N = 256 MMAs leave the tensor pipe room
+    // for the extra step, and the lighter reduction is what sets the pace.
+    constexpr bool kFold = KB <= 2;
+    constexpr uint32_t kNormBytes =
+        kFold ? kOnesBytes + kFoldStages * kFoldBlockBytes : kCnStages * NT * 4u;
     constexpr int kCW = NT / CH;
     constexpr int kChunks = kCW / 32;
     constexpr int kGroup = kChunks < 4 ? kChunks : 4;
@@ -374,7 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     const uint32_t x_base = base;
     const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
     const uint32_t cn_base = c_base + p.stages * kCStageBytes;
-    const uint32_t red_base = cn_base + kCnStages * NT * 4;
+    const uint32_t red_base = cn_base + kNormBytes;   // fold: ones tile, then fold slots
     const uint32_t snap_base = red_base + (CH - 1) * kTileM * 8;
     const uint32_t bar_base = snap_base + (kSnap ? kConsumerWarps * 4096u : 0u);
     uint8_t *const sbase = smem_raw + (base - raw);
@@ -405,12 +416,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
             mbar_init(bar(kBarCEmpty + s), 1);
         }
         for (int s = 0; s < kCnStages; ++s) {
-            mbar_init(bar(kBarCnFull + s), 32);
-            mbar_init(bar(kBarCnEmpty + s), kConsumerWarps);
+            // folded: the fold slots' full barriers count the leader's
+            // expect_tx and both CTAs' copied bytes; the pair MMA's commit
+            // frees a slot in both CTAs
+            mbar_init(bar(kBarCnFull + s), kFold ? 1 : 32);
+            mbar_init(bar(kBarCnEmpty + s), kFold ? 1 : kConsumerWarps);
         }
         *abort_flag = 0u;
         fence_mbar_init();
     }
+    if (kFold)
+        fold_init<kHalf>(cn_base);   // the ones tile (the slots are overwritten by copies)
     if (warp == kMmaWarp) {
         tmem_alloc_pair(smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
         tmem_relinquish_pair();
@@ -426,8 +442,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     if (warp == kProducerWarp) {
         if (lane == 0) {
             tma_prefetch_desc(&cmap);
+            if (kFold)
+                tma_prefetch_desc(&fmap);
             const uint64_t pol_c = policy_evict_last();
-            uint32_t stage = 0, phase = 0;
+            uint32_t stage = 0, phase = 0, fold_n = 0;
             bool ok = true;
             for (int u = cluster; ok && u < p.num_units; u += nclusters) {
                 const Unit w = decode_unit<2>(p, u);
@@ -446,6 +464,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                             stage = 0;
                             phase ^= 1u;
                         }
+                    }
+                    if (kFold && ok) {
+                        // this CTA's 128 centroids of the tile: fold block
+                        // 2 * tile + rank, 256 rows of 16 bytes
+                        const uint32_t fs = fold_n % kFoldStages;
+                        const uint32_t fph = (fold_n / kFoldStages) & 1u;
+                        if (!(ok = wait1(bar(kBarCnEmpty + fs), fph ^ 1u, abort_flag,
+                                         p.timeout_ns)))
+                            break;
+                        if (leader)
+                            mbar_arrive_expect_tx(bar(kBarCnFull + fs), 2 * kFoldBlockBytes);
+                        tma_load_2d_pair(cn_base + kOnesBytes + fs * kFoldBlockBytes, &fmap,
+                                         lead_bar(kBarCnFull + fs), 0,
+                                         (2 * tile + static_cast<int>(rank)) * 256, pol_c);
+                        ++fold_n;
                     }
                 }
             }
@@ -494,8 +527,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
         __syncwarp();
     } else if (warp == kMmaWarp) {
         if (leader) {
-            uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0;
+            uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0, fold_used = 0;
             bool ok = true, issued = false;
+            const uint64_t ones_desc = kFold ? plain_kmajor_desc(cn_base, kFoldLbo, kFoldSbo) : 0;
             for (int u = cluster; ok && u < p.num_units; u += nclusters) {
                 const Unit w = decode_unit<2>(p, u);
                 const uint32_t xb = x_used % p.xbufs;
@@ -536,6 +570,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                     }
                     if (!ok)
                         break;
+                    if (kFold) {
+                        const uint32_t fb = fold_used % kFoldStages;
+                        const uint32_t fph = (fold_used / kFoldStages) & 1u;
+                        if (!(ok = wait_warp(bar(kBarCnFull + fb), fph, abort_flag,
+                                             p.timeout_ns)))
+                            break;
+                        const uint64_t bdesc =
+                            plain_kmajor_desc(cn_base + kOnesBytes + fb * kFoldBlockBytes,
+                                              kFoldPairLbo, kFoldPairSbo);
+                        if (elect_one()) {
+                            mma_bf16_pair(d_tmem, ones_desc, bdesc, kIdesc, 1u);
+                            mma_commit_pair(bar(kBarCnEmpty + fb), kBoth);
+                        }
+                        __syncwarp();
+                        ++fold_used;
+                    }
                     if (elect_one())
                         mma_commit_pair(bar(kBarAccFull + as), kBoth);
                     __syncwarp();
@@ -556,11 +606,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
             }
         }
     } else if (warp == kNormWarp) {
+        // Folded, the norms come in with the fold operand: nothing to stage.
         float *const cn_smem = reinterpret_cast<float *>(sbase + (cn_base - base));
         const float kNaN = __int_as_float(0x7fc00000);
         uint32_t n = 0;
         bool ok = true;
-        for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+        for (int u = cluster; !kFold && ok && u < p.num_units; u += nclusters) {
             const Unit w = decode_unit<2>(p, u);
             for (int tile = w.t_begin; tile < w.t_end; ++tile, ++n) {
                 const uint32_t b = n % kCnStages;
@@ -589,7 +640,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
         bool ok = true;
         for (int u = cluster; u < p.num_units; u += nclusters) {
             const Unit w = decode_unit<2>(p, u);
-            float best = __int_as_float(0x7f800000);
+            // +inf for scores, -inf for folded t
+            float best = __int_as_float(kFold ? 0xff800000 : 0x7f800000);
             int bi = kNone;
             for (int tile = w.t_begin; tile < w.t_end; ++tile, ++acc_used) {
                 const uint32_t as = acc_used & 1u;
@@ -598,7 +650,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                 const uint32_t nph = (acc_used / kCnStages) & 1u;
                 if (ok)
                     ok = wait_warp(bar(kBarAccFull + as), aph, abort_flag, p.timeout_ns);
-                if (ok)
+                if (ok && !kFold)
                     ok = wait_warp(bar(kBarCnFull + nb), nph, abort_flag, p.timeout_ns);
                 if (ok) {
                     tc_fence_after();
@@ -626,21 +678,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                         float m[kGroup];
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c) {
-                            apply_norms(v[c], cn_tile + 128u * (g * kGroup + c));
-                            m[c] = chunk_min(v[c]);
+                            if (kFold) {
+                                m[c] = chunk_max(v[c]);
+                            } else {
+                                apply_norms(v[c], cn_tile + 128u * (g * kGroup + c));
+                                m[c] = chunk_min(v[c]);
+                            }
                         }
                         const int jg = tile * NT + col0 + g * kGroup * 32;
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c)
-                            fold_chunk<kSnap>(v[c], m[c], jg + 32 * c, best, bi, slot);
+                            fold_chunk<kSnap, kFold>(v[c], m[c], jg + 32 * c, best, bi, slot);
                     }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(bar(kBarCnEmpty + nb));
+                    if (!kFold) {
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(bar(kBarCnEmpty + nb));
+                    }
                 }
             }
             if (kSnap)
                 resolve_snapshot(best, bi, slot);
+            if (kFold)
+                best = -2.0f * best;   // t back to the score s (exact)
             const int lrow = q * 32 + lane;
             if (CH > 1) {
                 float *red_s = reinterpret_cast<float *>(sbase + (red_base - base));
@@ -703,28 +763,29 @@ cudaError_t prepare_pair(size_t smem)
 
 template <int CH, int KB>
 cudaError_t launch_pair(const AssignParams &p, const CUtensorMap &xmap, const CUtensorMap &cmap,
-                        int grid, size_t smem, cudaStream_t stream)
+                        const CUtensorMap &fmap, int grid, size_t smem, cudaStream_t stream)
 {
-    assign_pair_kernel<CH, KB><<<grid, 32 * (4 * CH + 4), smem, stream>>>(xmap, cmap, p);
+    assign_pair_kernel<CH, KB><<<grid, 32 * (4 * CH + 4), smem, stream>>>(xmap, cmap, fmap, p);
     return cudaGetLastError();
 }
 
 template <int CH>
 cudaError_t dispatch_pair_kb(bool prepare, int kb, const AssignParams *p, const CUtensorMap *xmap,
-                             const CUtensorMap *cmap, int grid, size_t smem, cudaStream_t stream)
+                             const CUtensorMap *cmap, const CUtensorMap *fmap, int grid,
+                             size_t smem, cudaStream_t stream)
 {
     // D <= 64 has no pair kernel: there the single-block kernels fold the
     // norms into the MMA, and every plan must give the same bits.
     switch (kb) {
     case 2:
         return prepare ? prepare_pair<CH, 2>(smem)
-                       : launch_pair<CH, 2>(*p, *xmap, *cmap, grid, smem, stream);
+                       : launch_pair<CH, 2>(*p, *xmap, *cmap, *fmap, grid, smem, stream);
     case 3:
         return prepare ? prepare_pair<CH, 3>(smem)
-                       : launch_pair<CH, 3>(*p, *xmap, *cmap, grid, smem, stream);
+                       : launch_pair<CH, 3>(*p, *xmap, *cmap, *fmap, grid, smem, stream);
     case 4:
         return prepare ? prepare_pair<CH, 4>(smem)
-                       : launch_pair<CH, 4>(*p, *xmap, *cmap, grid, smem, stream);
+                       : launch_pair<CH, 4>(*p, *xmap, *cmap, *fmap, grid, smem, stream);
     default:
         return cudaErrorInvalidValue;
     }
@@ -768,14 +829,14 @@ cudaError_t dispatch_kb(bool prepare, int kb, const AssignParams *p, const CUten
 }
 
 cudaError_t dispatch(bool prepare, const Variant &v, int kb, const AssignParams *p,
-                     const CUtensorMap *xmap, const CUtensorMap *cmap, int grid, size_t smem,
-                     cudaStream_t stream)
+                     const CUtensorMap *xmap, const CUtensorMap *cmap, const CUtensorMap *fmap,
+                     int grid, size_t smem, cudaStream_t stream)
 {
     if (v.pair) {
         if (v.ch == 2)
-            return dispatch_pair_kb<2>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+            return dispatch_pair_kb<2>(prepare, kb, p, xmap, cmap, fmap, grid, smem, stream);
         if (v.ch == 4)
-            return dispatch_pair_kb<4>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+            return dispatch_pair_kb<4>(prepare, kb, p, xmap, cmap, fmap, grid, smem, stream);
         return cudaErrorInvalidValue;
     }
     if (v.sub == 1 && v.nt == 128 && v.ch == 1)
@@ -791,6 +852,26 @@ cudaError_t dispatch(bool prepare, const Variant &v, int kb, const AssignParams 
     return cudaErrorInvalidValue;
 }
 
+// The CTA pair's fold operand for K centroids: blocks of 128 centroids, each
+// [K half][128 rows][16 bytes] (the unswizzled K-major layout of one K = 16
+// MMA step's B operand): half 0 row r holds the three bf16 parts of
+// -cnorm[j] / 2 for j = 128 b + r, then zeros; half 1 is zero.  Rows past K
+// hold NaN, so their scores never win.
+__global__ void __launch_bounds__(256)
+    fold_operand_kernel(const float *__restrict__ cnorm, int64_t K, int64_t nblocks,
+                        uint4 *__restrict__ out)
+{
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (j >= nblocks * 128)
+        return;
+    uint32_t w0, w1;
+    fold_split(j < K ? __ldg(cnorm + j) : __int_as_float(0x7fc00000), w0, w1);
+    const int64_t b = j >> 7;
+    const int64_t r = j & 127;
+    out[b * 256 + r] = make_uint4(w0, w1, 0u, 0u);
+    out[b * 256 + 128 + r] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
 
 const Variant kVariants[kNumVariants] = {{2, 128, 1, false}, {1, 256, 2, false},
@@ -801,9 +882,10 @@ const Variant kVariants[kNumVariants] = {{2, 128, 1, false}, {1, 256, 2, false},
 size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 {
     const size_t stage_rows = v.pair ? v.nt / 2 : v.nt;
-    const bool fold = !v.pair && kblocks == 1;   // the single-block kernel's kFold
+    const bool fold = assign_folds(v, kblocks);   // the kernels' kFold
+    const size_t fold_slot = v.pair ? kFoldBlockBytes : static_cast<size_t>(v.nt) * 32;
     const size_t norm_bytes =
-        fold ? kOnesBytes + static_cast<size_t>(kFoldStages) * v.nt * 32 : kCnStages * v.nt * 4;
+        fold ? kOnesBytes + static_cast<size_t>(kFoldStages) * fold_slot : kCnStages * v.nt * 4;
     return 1024 + static_cast<size_t>(xbufs) * v.sub * kblocks * kXTileBytes +
            static_cast<size_t>(stages) * stage_rows * 128 + norm_bytes +
            static_cast<size_t>(v.ch - 1) * v.sub * kTileM * 8 +
@@ -814,14 +896,14 @@ size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 
 cudaError_t assign_prepare(const Variant &v, int kblocks, size_t smem)
 {
-    return dispatch(true, v, kblocks, nullptr, nullptr, nullptr, 0, smem, nullptr);
+    return dispatch(true, v, kblocks, nullptr, nullptr, nullptr, nullptr, 0, smem, nullptr);
 }
 
 cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
-                          const CUtensorMap &xmap, const CUtensorMap &cmap, int grid, size_t smem,
-                          cudaStream_t stream)
+                          const CUtensorMap &xmap, const CUtensorMap &cmap,
+                          const CUtensorMap &fmap, int grid, size_t smem, cudaStream_t stream)
 {
-    return dispatch(false, v, kblocks, &p, &xmap, &cmap, grid, smem, stream);
+    return dispatch(false, v, kblocks, &p, &xmap, &cmap, &fmap, grid, smem, stream);
 }
 
 cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int *clusters)
@@ -852,6 +934,30 @@ cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int 
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
+}
+
+bool assign_folds(const Variant &v, int kblocks)
+{
+    return v.pair ? kblocks <= 2 : kblocks == 1;
+}
+
+int64_t fold_operand_blocks(int64_t K)
+{
+    return (K + 255) / 256 * 2;
+}
+
+size_t fold_operand_bytes(int64_t K)
+{
+    return static_cast<size_t>(fold_operand_blocks(K)) * kFoldBlockBytes;
+}
+
+cudaError_t launch_fold_operand(const float *cnorm, int64_t K, void *out, cudaStream_t stream)
+{
+    const int64_t nblocks = fold_operand_blocks(K);
+    const int64_t rows = nblocks * 128;
+    fold_operand_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(
+        cnorm, K, nblocks, static_cast<uint4 *>(out));
+    return cudaGetLastError();
 }
 
 cudaError_t status_read_and_clear(int *code)

@@ -56,9 +56,21 @@ size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs);
 cudaError_t assign_prepare(const Variant &v, int kblocks, size_t smem_bytes);
 // Clusters of the pair kernel that can be resident at once.
 cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int *clusters);
+// fmap: the fold operand's tensor map, read only by kernels that fold the
+// norms into the MMA through it (assign_folds on a CTA pair); others ignore it.
 cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
-                          const CUtensorMap &xmap, const CUtensorMap &cmap, int grid,
-                          size_t smem_bytes, cudaStream_t stream);
+                          const CUtensorMap &xmap, const CUtensorMap &cmap,
+                          const CUtensorMap &fmap, int grid, size_t smem_bytes,
+                          cudaStream_t stream);
+// Whether the shape's kernel folds the norms into the MMA (single-block
+// kernels at one k-block, CTA pairs at up to two).
+bool assign_folds(const Variant &v, int kblocks);
+// The CTA pair's fold operand: fold_operand_blocks(K) blocks of 128
+// centroids, 4 KiB each ([K half][128 rows][16 B] bf16), written from the
+// norms by launch_fold_operand (rows past K hold NaN).
+int64_t fold_operand_blocks(int64_t K);
+size_t fold_operand_bytes(int64_t K);
+cudaError_t launch_fold_operand(const float *cnorm, int64_t K, void *out, cudaStream_t stream);
 
 // The k-nearest kernel: one shape (256 points x 128 centroids per tile, 8
 // consumer warps), a sorted list of `list` in {4, 8, 16, 32} >= k candidates

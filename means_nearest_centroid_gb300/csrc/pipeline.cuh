@@ -49,6 +49,12 @@ constexpr int kFoldStages = 3;
 constexpr uint32_t kOnesBytes = 4096;                 // 128 rows x 16 columns of bf16 1.0
 constexpr uint32_t kFoldLbo = 128;                    // between the two core matrices along K
 constexpr uint32_t kFoldSbo = 256;                    // between 8-row groups
+// The CTA pair's fold operand comes from global memory by TMA, one block of
+// 128 centroids (4 KiB) per CTA and tile, laid out [K half][128 rows][16 B]:
+// the same unswizzled K-major core matrices with other offsets.
+constexpr uint32_t kFoldBlockBytes = 4096;
+constexpr uint32_t kFoldPairLbo = 2048;               // between the two K halves
+constexpr uint32_t kFoldPairSbo = 128;                // between 8-row groups
 constexpr uint32_t kConsumerBarrier = 1;              // named barrier id
 // Bound on the teardown waits after an abort (copies and MMAs in flight
 // always finish; this only guards against a hardware failure).
@@ -456,6 +462,26 @@ __device__ __forceinline__ uint32_t bf16_bits(float v)
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
 }
 
+// -c / 2 (c a centroid norm, NaN past K) split into three bf16 parts
+// h + m + l, each the rounding of what the previous parts leave, so that
+// the sum carries the fp32 value's 24 bits; w0 = h | m << 16, w1 = l: the
+// first three K positions of the centroid's fold-operand row.  A non-finite
+// value goes whole into h.
+__device__ __forceinline__ void fold_split(float c, uint32_t &w0, uint32_t &w1)
+{
+    const float v = -0.5f * c;
+    if (isfinite(v)) {
+        const float h = __bfloat162float(__float2bfloat16_rn(v));
+        const float r = v - h;
+        const float m = __bfloat162float(__float2bfloat16_rn(r));
+        w0 = bf16_bits(h) | (bf16_bits(m) << 16);
+        w1 = bf16_bits(r - m);
+    } else {
+        w0 = bf16_bits(v);
+        w1 = 0u;
+    }
+}
+
 // Norm warp with FOLD: per tile, -||c_j||^2 / 2 for its NT centroids (NaN
 // past K) split into three bf16 parts h + m + l (each the rounding of what
 // the previous parts leave, so the sum carries the fp32 value's 24 bits), at
@@ -509,19 +535,8 @@ __device__ __forceinline__ void fold_norm_role(const AssignParams &p, uint32_t f
         // split this tile's norms
         uint32_t w0[kPer], w1[kPer];
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            const float v = -0.5f * cur[e];
-            if (isfinite(v)) {
-                const float h = __bfloat162float(__float2bfloat16_rn(v));
-                const float r = v - h;
-                const float m = __bfloat162float(__float2bfloat16_rn(r));
-                w0[e] = bf16_bits(h) | (bf16_bits(m) << 16);
-                w1[e] = bf16_bits(r - m);
-            } else {
-                w0[e] = bf16_bits(v);
-                w1[e] = 0u;
-            }
-        }
+        for (int e = 0; e < kPer; ++e)
+            fold_split(cur[e], w0[e], w1[e]);
         const uint32_t b = n % kFoldStages;
         const uint32_t ph = (n / kFoldStages) & 1u;
         if (!wait_warp(bar(kBarCnEmpty + b), ph ^ 1u, abort_flag, p.timeout_ns))

@@ -54,12 +54,13 @@ def test_forced_split_is_honoured(dev, ks):
         assert p["split_row_tiles"] < 1024
 
 
-def test_pair_plans_exist_only_above_d64_and_are_chosen_above_d128(dev):
-    assert km.kmassign_plan(262144, 16384, 256)["rows_per_cta"] == 256
-    assert km.kmassign_plan(262144, 16384, 256)["centroids_per_tile"] == 256
-    assert km.kmassign_plan(262144, 8192, 192)["centroids_per_tile"] == 256
-    p128 = km.kmassign_plan(262144, 16384, 128)
-    assert not (p128["rows_per_cta"] == 256 and p128["centroids_per_tile"] == 256)
+def test_pair_plans_exist_only_above_d64_and_are_chosen_for_large_shapes(dev):
+    # above D = 128 the pair, at D = 96 and 128 the pair that folds the norms
+    for D in (256, 192, 128, 96):
+        p = km.kmassign_plan(262144, 16384, D)
+        assert (p["rows_per_cta"], p["centroids_per_tile"]) == (256, 256), D
+    p64 = km.kmassign_plan(262144, 16384, 64)
+    assert not (p64["rows_per_cta"] == 256 and p64["centroids_per_tile"] == 256)
     with pytest.raises(km.KmassignError):
         km.kmassign_plan(65536, 4096, 64, rows_per_cta=256, centroids_per_tile=256,
                          consumer_warps=8)

@@ -55,7 +55,13 @@ def test_noalloc_matches_kmassign_twice(dev, N, K, D, given, gen):
     cn = km.kmassign_norms(Cd) if given else None
     ref_idx = torch.empty(N, dtype=torch.int32, device=dev)
     ref_ms = torch.empty(N, dtype=torch.float32, device=dev)
-    km.kmassign(Xd, Cd, cnorm=cn, idx=ref_idx, minscore=ref_ms)
+    # Where kmassign would run the CTA pair that folds the norms (64 < D <=
+    # 128), this entry point has no room for its fold operand and runs the
+    # 256-row single-block shape: compare with that plan, bit for bit.
+    auto = km.kmassign_plan(N, K, D)
+    pair_fold = 64 < D <= 128 and (auto["rows_per_cta"], auto["centroids_per_tile"]) == (256, 256)
+    plan = dict(rows_per_cta=256, centroids_per_tile=128) if pair_fold else {}
+    km.kmassign_ex(Xd, Cd, cnorm=cn, idx=ref_idx, minscore=ref_ms, **plan)
     assert km.kmassign_check() == 0
     for _ in range(2):
         idx = torch.full((N,), -1, dtype=torch.int32, device=dev)
