@@ -679,7 +679,11 @@ def main():
                          f"{secs:.1f} s, fp64 oracle (OpenMP over points)"}
 
     clocks = sampler.summary(wall0, wall1)
-    launches_per_step = (1 if norms_in_step else 0) + 1 + (1 if plan["ksplit"] > 1 else 0)
+    # norms (when computed in the step), the fold operand (a CTA pair that
+    # folds the norms: D <= 128), the assignment, and the split rows' finalize
+    folding_pair = pair and D <= 128
+    launches_per_step = ((1 if norms_in_step else 0) + (1 if folding_pair else 0) + 1 +
+                         (1 if plan["ksplit"] > 1 else 0))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
