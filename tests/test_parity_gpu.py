@@ -149,6 +149,27 @@ def test_adversarial_reduced_bit_exact(dev):
         assert rep.ok() and rep.idx_mismatches == 0, (plan, rep)
 
 
+@pytest.mark.parametrize("D", [96, 128, 192, 256])
+def test_adversarial_specials_every_plan_wider_rows(dev, D):
+    """Ties, twins, all-equal centroids and rows with NaN, +-inf and -0 on
+    integer data at the widths the CTA pairs run (folding the norms up to
+    D = 128): every plan bit-exact against the oracle and against each other."""
+    N, K = 4000, 2048
+    X, C = workloads.adversarial(N, K, D, seed=D)
+    ref = None
+    for plan in plans_for(D):
+        idx, ms = run(dev, X, C, plan=plan)
+        rep = parity.compare(X, C, idx, ms, integer=True)
+        assert rep.ok() and rep.idx_mismatches == 0, (plan, rep)
+        nan_rows = torch.isnan(X.float()).any(1)
+        assert bool((idx[nan_rows] == 0).all()) and bool(torch.isnan(ms[nan_rows]).all()), plan
+        if ref is None:
+            ref = (idx, ms)
+            continue
+        assert torch.equal(idx, ref[0]), plan
+        assert torch.equal(ms.view(torch.int32), ref[1].view(torch.int32)), plan
+
+
 def test_plans_give_identical_bits_on_float_data(dev):
     """D = 128: the single-block plans agree bit for bit, and so do the
     folding CTA-pair plans; both classes pass the oracle."""
