@@ -103,8 +103,8 @@ int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_
  *   rows_per_cta        128 or 256 points per work unit
  *   centroids_per_tile  128 or 256 centroids per tensor-core tile; 256 with
  *                       256 rows selects the CTA-pair kernel (two thread
- *                       blocks on two SMs share each 256x256 tile; D > 64
- *                       only)
+ *                       blocks on two SMs share each 256x256 tile; at
+ *                       D <= 128 it folds the norms into the MMA)
  *   consumer_warps      warps reducing the score tiles per thread block: 4
  *                       (128x128 tiles), 8 or 16 (all other shapes)
  * Same arguments, layout and errors as kmassign; a value outside these sets,

@@ -48,7 +48,7 @@ int current_device_info(DeviceInfo *out)
                 cudaSuccess)
             return KMASSIGN_ERR_CUDA;
         for (const auto &v : kma::kVariants)
-            for (int kb = v.pair ? 2 : 1; kb <= 4; ++kb)   // pair kernels: D > 64 only
+            for (int kb = 1; kb <= 4; ++kb)
                 if (kma::assign_prepare(v, kb, static_cast<size_t>(d.smem_optin)) != cudaSuccess)
                     return KMASSIGN_ERR_CUDA;
         for (int list = 4; list <= 32; list *= 2)
@@ -232,8 +232,8 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
             continue;
         if (force_cw != 0 && force_cw != 4 * v.sub * v.ch)
             continue;
-        if (v.pair && (dev.pair_clusters < 1 || kblocks <= 1))
-            continue;   // pair kernels exist for D > 64 only
+        if (v.pair && dev.pair_clusters < 1)
+            continue;
         const int64_t P = v.pair ? dev.pair_clusters : dev.sms;   // units run in parallel
         const size_t xbytes = static_cast<size_t>(v.sub) * kblocks * kma::kXTileBytes;
         const size_t stage_bytes = static_cast<size_t>(v.pair ? v.nt / 2 : v.nt) * 128;
@@ -249,15 +249,16 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const double mma_clk = v.nt == 256 ? 128.0 : (v.sub == 2 ? 80.0 : 92.0);
         // Kernels that fold the norms into one more MMA step (single-block
         // at D <= 64, CTA pairs at D <= 128) have a lighter reduction
-        // (256x128 tiles: ~1250 clocks with 8 warps, ~1600 with 16, measured
-        // at D = 64; a CTA pair's 128x256 per SM: ~1450 with 8 warps,
-        // measured at D = 128 against 1,780 for the 256x128 single block).
+        // (256x128 single-block tiles at D = 64: ~1,500 clocks with 8 warps,
+        // ~1,600 with 16; a CTA pair's 128x256 per SM: ~1,390 at D = 64 and
+        // ~1,420 at D = 128, against ~1,780 for the 256x128 single block at
+        // D = 128).
         const bool fold = !topk && kma::assign_folds(v, kblocks);
         const double tile_mma = double(v.sub) * (kblocks * 4 + (fold ? 1 : 0)) * mma_clk + 500.0;
         const double tile_epi =
             (v.pair && fold)
                 ? (v.ch == 2 ? 1450.0 : 1600.0)
-                : fold ? (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1600.0 : 1250.0) : 1400.0)
+                : fold ? (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1600.0 : 1500.0) : 1400.0)
                        : (v.nt == 256 ? 2150.0 : v.sub == 2 ? (v.ch == 2 ? 1550.0 : 1700.0)
                                                             : 1400.0);
         // The pair kernel halves each SM's C traffic but couples both SMs'
@@ -268,11 +269,11 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         // cap (less L2 traffic per flop).  At D <= 128 it folds, modelled
         // by its reduction floor above.
         const double pair_factor = kblocks >= 3 ? 0.94 : 1.0;
-        // A folding pair's tile measured ~1,420 clocks (8 warps) at D = 128,
-        // below its modelled MMA time; its fold operand costs one small
-        // kernel per call.
+        // A folding pair's tile is its measured time (8 warps: ~1,390 clocks
+        // at D = 64, ~1,420 at D = 128), below its modelled MMA time; its
+        // fold operand costs one small kernel per call.
         const bool pair_fold = v.pair && fold;
-        const double tile = pair_fold ? (v.ch == 2 ? 1420.0 : 1600.0)
+        const double tile = pair_fold ? (v.ch == 2 ? (kblocks == 1 ? 1390.0 : 1420.0) : 1600.0)
                                       : std::max(tile_mma, tile_epi) * (v.pair ? pair_factor : 1.0);
         const double call_over = pair_fold ? 6000.0 : 0.0;
         const double unit_over = 5000.0;

@@ -774,9 +774,10 @@ cudaError_t dispatch_pair_kb(bool prepare, int kb, const AssignParams *p, const 
                              const CUtensorMap *cmap, const CUtensorMap *fmap, int grid,
                              size_t smem, cudaStream_t stream)
 {
-    // D <= 64 has no pair kernel: there the single-block kernels fold the
-    // norms into the MMA, and every plan must give the same bits.
     switch (kb) {
+    case 1:
+        return prepare ? prepare_pair<CH, 1>(smem)
+                       : launch_pair<CH, 1>(*p, *xmap, *cmap, *fmap, grid, smem, stream);
     case 2:
         return prepare ? prepare_pair<CH, 2>(smem)
                        : launch_pair<CH, 2>(*p, *xmap, *cmap, *fmap, grid, smem, stream);
@@ -908,19 +909,21 @@ cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
 
 cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int *clusters)
 {
-    if (kblocks < 2 || kblocks > 4)
+    if (kblocks < 1 || kblocks > 4)
         return cudaErrorInvalidValue;
     const void *fn = nullptr;
     if (v.ch == 2) {
-        const void *t[3] = {(const void *)assign_pair_kernel<2, 2>,
+        const void *t[4] = {(const void *)assign_pair_kernel<2, 1>,
+                            (const void *)assign_pair_kernel<2, 2>,
                             (const void *)assign_pair_kernel<2, 3>,
                             (const void *)assign_pair_kernel<2, 4>};
-        fn = t[kblocks - 2];
+        fn = t[kblocks - 1];
     } else {
-        const void *t[3] = {(const void *)assign_pair_kernel<4, 2>,
+        const void *t[4] = {(const void *)assign_pair_kernel<4, 1>,
+                            (const void *)assign_pair_kernel<4, 2>,
                             (const void *)assign_pair_kernel<4, 3>,
                             (const void *)assign_pair_kernel<4, 4>};
-        fn = t[kblocks - 2];
+        fn = t[kblocks - 1];
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);

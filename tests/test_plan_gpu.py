@@ -54,16 +54,19 @@ def test_forced_split_is_honoured(dev, ks):
         assert p["split_row_tiles"] < 1024
 
 
-def test_pair_plans_exist_only_above_d64_and_are_chosen_for_large_shapes(dev):
-    # above D = 128 the pair, at D = 96 and 128 the pair that folds the norms
-    for D in (256, 192, 128, 96):
+def test_pair_plans_are_chosen_for_large_shapes(dev):
+    # above D = 128 the pair; up to D = 128 the pair that folds the norms,
+    # where enough tiles per unit amortise its fold operand
+    for D in (256, 192, 128, 96, 64):
         p = km.kmassign_plan(262144, 16384, D)
         assert (p["rows_per_cta"], p["centroids_per_tile"]) == (256, 256), D
-    p64 = km.kmassign_plan(262144, 16384, 64)
-    assert not (p64["rows_per_cta"] == 256 and p64["centroids_per_tile"] == 256)
-    with pytest.raises(km.KmassignError):
-        km.kmassign_plan(65536, 4096, 64, rows_per_cta=256, centroids_per_tile=256,
+    # short centroid ranges at D = 64 stay on the single-block fold
+    p = km.kmassign_plan(262144, 4096, 64)
+    assert (p["rows_per_cta"], p["centroids_per_tile"]) == (256, 128)
+    # every shape can be forced at any D
+    p = km.kmassign_plan(65536, 4096, 32, rows_per_cta=256, centroids_per_tile=256,
                          consumer_warps=8)
+    assert (p["rows_per_cta"], p["centroids_per_tile"]) == (256, 256)
 
 
 def test_plan_ex_rejects_bad_forcing(dev):
