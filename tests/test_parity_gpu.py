@@ -352,3 +352,31 @@ def test_invalid_tail_value_rejected(dev):
     X, C = workloads.iid(10, 4, 64, seed=2)
     with pytest.raises(km.KmassignError):
         km.kmassign_ex(X.to(dev), C.to(dev), ksplit=-1)
+
+
+# ---------------------------------------------------------------- random shapes
+def _random_cases(n, seed=2026):
+    g = np.random.default_rng(seed)
+    cases = []
+    for c in range(n):
+        N = int(g.integers(1, 3000))
+        K = int(g.integers(1, 5000))
+        D = int(g.choice([16, 32, 48, 64, 80, 96, 112, 128, 160, 192, 224, 256]))
+        plan = PLANS[int(g.integers(0, len(PLANS)))]
+        cases.append((N, K, D, plan))
+    return cases
+
+
+@pytest.mark.parametrize("N,K,D,plan", _random_cases(40), ids=str)
+def test_random_shapes_and_plans(dev, N, K, D, plan):
+    """Seeded random ragged shapes on a random forced plan (every shape runs
+    at every D): integer data bit-exact against the oracle, float data within
+    the tolerance."""
+    Xi, Ci = workloads.integers(N, K, D, seed=N * 3 + K + D)
+    idx, ms = run(dev, Xi, Ci, plan=plan)
+    rep = parity.compare(Xi, Ci, idx, ms, integer=True)
+    assert rep.ok() and rep.idx_mismatches == 0, (plan, rep)
+    X, C = workloads.blobs(N, K, D, seed=N + K * 3 + D)
+    idx, ms = run(dev, X, C, plan=plan)
+    rep = parity.compare(X, C, idx, ms)
+    assert rep.ok(), (plan, rep)
