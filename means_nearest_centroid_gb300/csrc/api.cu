@@ -193,12 +193,15 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 // (the five benchmark workloads, every shape forced in turn):
 //   * tensor pipe: a 128x256x16 bf16 MMA takes 128 clocks back to back, a
 //     128x128x16 one ~80 with two accumulators and ~92 with one, plus ~500
-//     clocks of hand-over per tile (D <= 64: one more MMA per tile, the
-//     folded norms);
+//     clocks of hand-over per tile (with folded norms one more MMA step);
 //   * epilogue floor per tile (latency-bound reduction): ~2150 clocks for a
 //     128x256 tile with 8 or 16 warps, ~1700 / ~1550 for a 256x128 tile with
-//     8 / 16 warps (~1250 / ~1600 with folded norms), ~1400 for a 128x128
+//     8 / 16 warps (~1500 / ~1600 with folded norms), ~1400 for a 128x128
 //     tile with 4 warps;
+//   * a CTA pair costs its measured tile time: above D = 128 the larger of
+//     its MMA time and floor, scaled by 0.94; at D <= 128, where it folds,
+//     ~1390 (D = 64) / ~1420 (D = 128) clocks with 8 warps, plus ~6000
+//     clocks per call for the fold operand;
 //   * a unit pays ~5000 clocks to load its X tile and fill the pipe;
 //   * any split pays ~12000 clocks for the key memset, the finalize kernel
 //     and their launches.

@@ -337,8 +337,11 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
 // same shared memory.  The leader CTA (rank 0) issues the pair MMAs; their
 // completion is multicast to both CTAs' barriers; the peer's copies count on
 // the leader's full barriers and its consumers hand accumulator stages back
-// by arriving on the leader's empty barriers.  Everything else (norm ring,
-// reduction, stores) is per CTA and identical to the single-CTA kernel.
+// by arriving on the leader's empty barriers.  At D <= 128 the pair folds the
+// norms into the MMA (one more step per tile, its B operand TMA-loaded from a
+// precomputed fold operand like a C k-block); above, a norm ring serves the
+// epilogue as in the single-CTA kernel.  The reduction and the stores are per
+// CTA and identical to the single-CTA kernel's.
 template <int CH, int KB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1)
     assign_pair_kernel(const __grid_constant__ CUtensorMap xmap,

@@ -40,11 +40,12 @@ constexpr int kBarCnFull = kBarCEmpty + kMaxStages;   // [kCnStages]
 constexpr int kBarCnEmpty = kBarCnFull + kCnStages;   // [kCnStages]
 constexpr int kNumBars = kBarCnEmpty + kCnStages;
 constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot + abort flag
-// Norm folding (D <= 64): the norms enter the accumulator through one more
-// K = 16 MMA step per tile, A = a constant tile of ones, B = the tile's
-// -||c||^2 / 2 split into three bf16 parts.  Shared memory: the ones tile,
-// then kFoldStages slots of NT rows x 32 bytes (plain K-major layout: 8-row
-// groups of 256 bytes, each two 128-byte core matrices along K).
+// Norm folding (single-block kernels at D <= 64, CTA pairs at D <= 128): the
+// norms enter the accumulator through one more K = 16 MMA step per tile,
+// A = a constant tile of ones, B = the tile's -||c||^2 / 2 split into three
+// bf16 parts.  Single-block shared memory: the ones tile, then kFoldStages
+// slots of NT rows x 32 bytes (plain K-major layout: 8-row groups of 256
+// bytes, each two 128-byte core matrices along K) that a norm warp fills.
 constexpr int kFoldStages = 3;
 constexpr uint32_t kOnesBytes = 4096;                 // 128 rows x 16 columns of bf16 1.0
 constexpr uint32_t kFoldLbo = 128;                    // between the two core matrices along K
