@@ -150,28 +150,33 @@ struct TopList {
 // The chunk is first copied to this thread's shared slot (float4 i at
 // slot + 512 i, conflict-free across the warp), so each marked column is one
 // shared load instead of a 31-select tree.
+//
+// The accumulators hold the folded t = x.c - ||c||^2 / 2 = -s / 2 (the norms
+// enter through one more MMA step), so the tests run on t: s < thr exactly
+// when t > tthr = -thr / 2, and a candidate's score is s = -2 t (both exact).
+// mt is the chunk's largest t (NaN only if every t is NaN).
 template <int L>
-__device__ __forceinline__ void admit_chunk(TopList<L> &lst, const float (&s)[32], float m,
-                                            int j0, float &thr, uint32_t slot)
+__device__ __forceinline__ void admit_chunk(TopList<L> &lst, const float (&t)[32], float mt,
+                                            int j0, float &tthr, uint32_t slot)
 {
-    if (m != m && lst.o[L - 1] == kNaNOrd)
+    if (mt != mt && lst.o[L - 1] == kNaNOrd)
         return;
     uint32_t mask = 0;
 #pragma unroll
     for (int e = 0; e < 32; ++e)
-        mask |= (s[e] >= thr) ? 0u : (1u << e);
+        mask |= (t[e] <= tthr) ? 0u : (1u << e);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        st_shared_v4(slot + 512u * i, s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+        st_shared_v4(slot + 512u * i, t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
     while (mask != 0u) {
         const int e = __ffs(mask) - 1;
         mask &= mask - 1u;
-        const uint32_t u =
-            ord_of(lds_f32(slot + 512u * static_cast<uint32_t>(e >> 2) + 4u * (e & 3)));
+        const uint32_t u = ord_of(
+            -2.0f * lds_f32(slot + 512u * static_cast<uint32_t>(e >> 2) + 4u * (e & 3)));
         if (u < lst.o[L - 1])
             lst.push_later(u, j0 + e);
     }
-    thr = of_ord(lst.o[L - 1]);
+    tthr = -0.5f * of_ord(lst.o[L - 1]);
 }
 
 template <int KB, int L>
@@ -204,9 +209,9 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
     const uint32_t x_base = base;
     const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
     const uint32_t cn_base = c_base + p.stages * kCStageBytes;   // float[kCnStages][NT]
-    const uint32_t snap_base = cn_base + kCnStages * NT * 4;   // [warp][8][32] float4
+    // folded norms: the ones tile, then the fold slots the norm warp fills
+    const uint32_t snap_base = cn_base + kOnesBytes + kFoldStages * NT * 32u;   // [warp][8][32] float4
     const uint32_t bar_base = snap_base + kConsumerWarps * 4096u;
-    uint8_t *const sbase = smem_raw + (base - raw);
     uint8_t *misc_ptr = smem_raw + (bar_base - raw) + kNumBars * 8;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(misc_ptr);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(misc_ptr + 4);
@@ -216,7 +221,8 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0)
-        init_barriers<kConsumerWarps>(bar_base, abort_flag);
+        init_barriers<kConsumerWarps, true>(bar_base, abort_flag);
+    fold_init<NT>(cn_base);
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
         tmem_relinquish();
@@ -231,10 +237,9 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
     } else if (warp == kXWarp) {
         x_role<SUB, KB>(p, &xmap, x_base, bar_base, abort_flag);
     } else if (warp == kMmaWarp) {
-        mma_role<SUB, NT, KB>(p, x_base, c_base, bar_base, tmem_base, abort_flag);
+        mma_role<SUB, NT, KB, true>(p, x_base, c_base, bar_base, tmem_base, abort_flag, cn_base);
     } else if (warp == kNormWarp) {
-        norm_role<SUB, NT>(p, reinterpret_cast<float *>(sbase + (cn_base - base)), bar_base,
-                           abort_flag);
+        fold_norm_role<SUB, NT>(p, cn_base, bar_base, abort_flag);
     } else {
         // Consumer warp w reads TMEM lanes 32*(w%4) .. +31 of sub-tile w/4,
         // every column of every tile.
@@ -249,21 +254,16 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
             const Unit w = decode_unit<SUB>(p, u);
             TopList<L> lst;
             lst.clear();
-            float thr = __int_as_float(0x7fc00000);
+            float tthr = __int_as_float(0x7fc00000);   // -(the list's last score) / 2
             for (int tile = w.t_begin; tile < w.t_end; ++tile, ++acc_used) {
                 const uint32_t as = acc_used & 1u;
                 const uint32_t aph = (acc_used >> 1) & 1u;
-                const uint32_t nb = acc_used % kCnStages;
-                const uint32_t nph = (acc_used / kCnStages) & 1u;
                 if (ok)
                     ok = wait_warp(bar(kBarAccFull + as), aph, abort_flag, p.timeout_ns);
-                if (ok)
-                    ok = wait_warp(bar(kBarCnFull + nb), nph, abort_flag, p.timeout_ns);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                            as * kAccCols + t * NT;
-                    const uint32_t cn_tile = cn_base + 4u * NT * nb;
 #pragma unroll
                     for (int g = 0; g < kGroups; ++g) {
                         __syncwarp();   // tcgen05.ld is .sync.aligned
@@ -281,19 +281,14 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
                         }
                         float m[kGroup];
 #pragma unroll
-                        for (int c = 0; c < kGroup; ++c) {
-                            apply_norms(v[c], cn_tile + 128u * (g * kGroup + c));
-                            m[c] = chunk_min(v[c]);
-                        }
+                        for (int c = 0; c < kGroup; ++c)
+                            m[c] = chunk_max(v[c]);
                         const int jg = tile * NT + g * kGroup * 32;
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c)
-                            if (!(m[c] >= thr))
-                                admit_chunk<L>(lst, v[c], m[c], jg + 32 * c, thr, slot);
+                            if (!(m[c] <= tthr))
+                                admit_chunk<L>(lst, v[c], m[c], jg + 32 * c, tthr, slot);
                     }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(bar(kBarCnEmpty + nb));
                 }
             }
 
@@ -466,7 +461,7 @@ int topk_list_size(int k)
 size_t topk_smem_bytes(int kblocks, int stages, int xbufs)
 {
     return 1024 + static_cast<size_t>(xbufs) * kTopSub * kblocks * kXTileBytes +
-           static_cast<size_t>(stages) * kTopNt * 128 + kCnStages * kTopNt * 4 +
+           static_cast<size_t>(stages) * kTopNt * 128 + kOnesBytes + kFoldStages * kTopNt * 32 +
            static_cast<size_t>(kTopConsumerWarps) * 4096 + kMiscBytes;
 }
 
