@@ -149,7 +149,7 @@ int kmassign_check(void *stream);
  * its memory budget at start-up because cudaMalloc/cudaFree can synchronise
  * the device.
  *
- * Same arguments, layout, results and errors as kmassign.  Its temporaries
+ * Same arguments, layout, results (but see below) and errors as kmassign.  Its temporaries
  * live in one static device array of this library (6 MiB, held on every GPU
  * that loads the library until the process exits) instead of the stream
  * allocator; it calls no cudaMalloc, cudaFree or other allocating routine.
@@ -157,6 +157,11 @@ int kmassign_check(void *stream);
  *     larger K returns KMASSIGN_ERR_SCRATCH before anything is launched.
  *   - A split centroid range keeps one 8-byte key per point in the array;
  *     for N > 262,144 the call plans without a split instead.
+ *   - Where kmassign would run CTA pairs that fold the norms into the MMA
+ *     (64 < D <= 128) and need a fold operand in memory, this call runs the
+ *     256-row single-block tiles instead: on float data its minscore (and,
+ *     at near ties, idx) can differ from kmassign's in the last bits, both
+ *     within the same tolerance of the exact scores; integer data agree.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call shares the one array and overwrites
