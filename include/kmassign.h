@@ -16,15 +16,27 @@
  * scores are all NaN (for example a row holding a NaN) gets idx 0 and minscore
  * NaN; the pages test NaN rows but fix no convention, this is the one chosen.
  *
- * Arithmetic (what the GPU computes): x and c are bf16; x_i . c_j is summed in
- * fp32 by the tensor cores (order of summation unspecified); ||c_j||^2 is an
- * fp32 sum of exact bf16 squares; s_ij = fmaf(-2, dot, cnorm_j) in fp32.  On
- * integer-valued inputs whose sums stay below 2^24 every step is exact.
+ * Arithmetic (what the GPU computes): x and c are bf16; ||c_j||^2 is an fp32
+ * sum of exact bf16 squares (or the caller's cnorm).  The tensor cores sum in
+ * fp32, in an order the hardware fixes:
+ *   - D <= 128: the accumulator takes x_i . c_j and then -||c_j||^2 / 2,
+ *     entered as three bf16 parts h + m + l that carry all 24 bits of the
+ *     fp32 value (one more K = 16 tensor-core step, A = ones), so it holds
+ *     t_ij = x_i . c_j - ||c_j||^2 / 2; the winner is the largest t and
+ *     s_ij = -2 t_ij (exact);
+ *   - D > 128: the accumulator holds x_i . c_j and s_ij = fmaf(-2, dot,
+ *     cnorm_j) in fp32.
+ * Which of the two applies depends on D alone: every plan, batch size and
+ * split gives a point the same idx and minscore bits.  On integer-valued
+ * inputs whose sums stay below 2^24 every step is exact.
  *
  * Layout: every matrix is row-major and contiguous, D innermost.  Row pitch
  * is D * 2 bytes.  All pointers are device pointers (cudaMalloc, the stream
  * allocator or PyTorch CUDA tensors); host or unregistered pointers are
  * rejected with KMASSIGN_ERR_NOT_DEVICE before anything is launched.
+ *
+ * Devices: the pointers' device is made current for the launches; the calling
+ * thread's current device is restored before every entry point returns.
  *
  * Ownership: the caller owns every buffer it passes.  The library keeps no
  * pointer after a call returns.  Temporaries (the norm buffer when cnorm is
@@ -83,11 +95,12 @@ int kmassign_norms(const void *C, int64_t K, int64_t D, float *cnorm, void *stre
  *   K         1 <= K < 2^31
  *   D         multiple of 16 in [16, 256]
  *   idx       device int32 [N], written
- *   minscore  device fp32 [N] or NULL; when given, the winning score
- *             fmaf(-2, dot, cnorm[idx]) with -0 written as +0, or NaN for an
+ *   minscore  device fp32 [N] or NULL; when given, the winning score s
+ *             computed as above, with -0 written as +0, or NaN for an
  *             all-NaN row
- * The result does not depend on how the work is tiled or split: every plan
- * returns the same idx and minscore bits.
+ * The result does not depend on how the work is tiled or split, nor on the
+ * other points of the call: every plan returns the same idx and minscore
+ * bits, and a point assigned alone gets the bits it gets in any batch.
  */
 int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
              int64_t D, int32_t *idx, float *minscore, void *stream);
@@ -104,7 +117,7 @@ int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_
  *   centroids_per_tile  128 or 256 centroids per tensor-core tile; 256 with
  *                       256 rows selects the CTA-pair kernel (two thread
  *                       blocks on two SMs share each 256x256 tile; at
- *                       D <= 128 it folds the norms into the MMA)
+ *                       D <= 128 every shape folds the norms into the MMA)
  *   consumer_warps      warps reducing the score tiles per thread block: 4
  *                       (128x128 tiles), 8 or 16 (all other shapes)
  * Same arguments, layout and errors as kmassign; a value outside these sets,
@@ -138,6 +151,9 @@ int kmassign_plan_ex(int64_t N, int64_t K, int64_t D, int ksplit, int rows_per_c
  * Synchronise `stream`, then report and clear the device status word:
  * KMASSIGN_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
  * check, KMASSIGN_ERR_CUDA if the stream reports an error, else KMASSIGN_OK.
+ * The status word belongs to the current device and is shared by every
+ * stream and thread of the process: a timeout raised by a kernel on one
+ * stream is reported, and cleared, by a check on any stream of that device.
  */
 int kmassign_check(void *stream);
 
@@ -149,7 +165,7 @@ int kmassign_check(void *stream);
  * its memory budget at start-up because cudaMalloc/cudaFree can synchronise
  * the device.
  *
- * Same arguments, layout, results (but see below) and errors as kmassign.  Its temporaries
+ * Same arguments, layout, results (bit for bit) and errors as kmassign.  Its temporaries
  * live in one static device array of this library (6 MiB, held on every GPU
  * that loads the library until the process exits) instead of the stream
  * allocator; it calls no cudaMalloc, cudaFree or other allocating routine.
@@ -158,13 +174,13 @@ int kmassign_check(void *stream);
  *   - A split centroid range keeps one 8-byte key per point in the array;
  *     for N > 262,144 the call plans without a split instead.
  *   - Where kmassign would run CTA pairs that fold the norms into the MMA
- *     (64 < D <= 128) and need a fold operand in memory, this call runs the
- *     256-row single-block tiles instead: on float data its minscore (and,
- *     at near ties, idx) can differ from kmassign's in the last bits, both
- *     within the same tolerance of the exact scores; integer data agree.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call shares the one array and overwrites
+ *     (every D <= 128) and read a fold operand from memory, this call plans
+ *     without CTA pairs; every plan gives the same bits, so the results are
+ *     still kmassign's.
+ * The first call on a device does that device's set-up with it current: the
+ * kernels' shared-memory attributes, the library's memory pool (used only by
+ * the other entry points) and the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.  Every call shares the one array and overwrites
  * what the previous call left there, so calls whose work overlaps on the GPU
  * (different streams, or different host threads) race; order them on one
  * stream or synchronise between them.
@@ -235,9 +251,11 @@ int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int 
  *   idx        device int32 [N, k] row-major, written: row i ascending
  *   score      device fp32 [N, k] row-major, or NULL (then distances must be
  *              0); written in idx's order:
- *                distances == 0: s_ij as kmassign's minscore computes it
- *                                (fp32 fma of the fp32 dot and norm, -0 as
- *                                +0, NaN for a NaN score)
+ *                distances == 0: s_ij = -2 t_ij from an accumulator that
+ *                                folds the norms in (as kmassign does at
+ *                                D <= 128, here at every D; k = 1 returns
+ *                                kmassign's minscore), -0 as +0, NaN for a
+ *                                NaN score
  *                distances == 1: ||x_i||^2 + s_ij in fp32 with ||x_i||^2 the
  *                                fp32 sum of exact bf16 squares, a negative
  *                                result (rounding) written as 0.  For

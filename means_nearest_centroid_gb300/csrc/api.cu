@@ -135,7 +135,8 @@ bool aligned(const void *p, uintptr_t a)
 // Host or foreign pointers would make the copy engine fault: reject them.
 // Every non-NULL pointer must be device (or managed) memory of one device;
 // that device is made current for this library's runtime before launching
-// (the caller's framework may track its current device separately).
+// (the caller's framework may track its current device separately), and the
+// entry point's DeviceRestore puts the caller's current device back.
 int check_device_ptrs(const void *const *ptrs, int n)
 {
     int owner = -1;
@@ -164,6 +165,31 @@ int check_device_ptrs(const void *const *ptrs, int n)
     }
     return KMASSIGN_OK;
 }
+
+// Puts back the calling thread's current device when an entry point returns
+// (check_device_ptrs makes the pointers' device current for the launches;
+// the caller's own notion of its current device must not change).
+class DeviceRestore {
+public:
+    DeviceRestore()
+    {
+        if (cudaGetDevice(&dev_) != cudaSuccess) {
+            cudaGetLastError();
+            dev_ = -1;
+        }
+    }
+    ~DeviceRestore()
+    {
+        int cur = -1;
+        if (dev_ >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != dev_)
+            cudaSetDevice(dev_);
+    }
+    DeviceRestore(const DeviceRestore &) = delete;
+    DeviceRestore &operator=(const DeviceRestore &) = delete;
+
+private:
+    int dev_ = -1;
+};
 
 int check_shape(int64_t N, int64_t K, int64_t D)
 {
@@ -214,7 +240,8 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 // the data and is taken as the assignment's, which only matters for choosing
 // the split.
 int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_ksplit,
-              int force_rows, int force_nt, int force_cw, bool topk, Plan *out)
+              int force_rows, int force_nt, int force_cw, bool topk, Plan *out,
+              bool no_pair = false)
 {
     auto smem_of = [&](const kma::Variant &v, int kblocks, int stages, int xbufs) {
         return topk ? kma::topk_smem_bytes(kblocks, stages, xbufs)
@@ -235,18 +262,19 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
             continue;
         if (force_cw != 0 && force_cw != 4 * v.sub * v.ch)
             continue;
-        if (v.pair && dev.pair_clusters < 1)
+        if (v.pair && (dev.pair_clusters < 1 || no_pair))
             continue;
         const int64_t P = v.pair ? dev.pair_clusters : dev.sms;   // units run in parallel
-        const size_t xbytes = static_cast<size_t>(v.sub) * kblocks * kma::kXTileBytes;
-        const size_t stage_bytes = static_cast<size_t>(v.pair ? v.nt / 2 : v.nt) * 128;
-        const size_t fixed = smem_of(v, kblocks, 0, 0);
+        // Shared memory: at least 2 ring stages and one X buffer; two X
+        // buffers when 4 stages still fit; then as many stages as fit.
         const size_t budget = static_cast<size_t>(dev.smem_optin);
-        if (fixed + xbytes + 2 * stage_bytes > budget)
+        auto fits = [&](int st, int xb) { return smem_of(v, kblocks, st, xb) <= budget; };
+        if (!fits(2, 1))
             continue;
-        const int xbufs = (fixed + 2 * xbytes + 4 * stage_bytes <= budget) ? 2 : 1;
-        const int stages = static_cast<int>(std::min<size_t>(
-            kma::kMaxStages, (budget - fixed - xbufs * xbytes) / stage_bytes));
+        const int xbufs = fits(4, 2) ? 2 : 1;
+        int stages = 2;
+        while (stages < kma::kMaxStages && fits(stages + 1, xbufs))
+            ++stages;
         const int64_t ntiles = cdiv(K, v.nt);
         const int64_t R = cdiv(N, static_cast<int64_t>(rows));
         const double mma_clk = v.nt == 256 ? 128.0 : (v.sub == 2 ? 80.0 : 92.0);
@@ -352,11 +380,12 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
 struct PlanKey {
     int64_t N, K, D;
     int ksplit, rows, nt, cw, dev;
-    bool topk;
+    bool topk, no_pair;
     bool operator==(const PlanKey &o) const
     {
         return N == o.N && K == o.K && D == o.D && ksplit == o.ksplit && rows == o.rows &&
-               nt == o.nt && cw == o.cw && dev == o.dev && topk == o.topk;
+               nt == o.nt && cw == o.cw && dev == o.dev && topk == o.topk &&
+               no_pair == o.no_pair;
     }
 };
 constexpr int kPlanCacheSize = 64;
@@ -365,9 +394,9 @@ Plan g_plans[kPlanCacheSize];
 int g_plan_count = 0, g_plan_next = 0;
 
 int cached_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int dev_id, int ksplit,
-                int rows, int nt, int cw, Plan *out, bool topk = false)
+                int rows, int nt, int cw, Plan *out, bool topk = false, bool no_pair = false)
 {
-    const PlanKey key{N, K, D, ksplit, rows, nt, cw, dev_id, topk};
+    const PlanKey key{N, K, D, ksplit, rows, nt, cw, dev_id, topk, no_pair};
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         for (int i = 0; i < g_plan_count; ++i)
@@ -376,7 +405,7 @@ int cached_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int dev_
                 return KMASSIGN_OK;
             }
     }
-    const int rc = make_plan(N, K, D, dev, ksplit, rows, nt, cw, topk, out);
+    const int rc = make_plan(N, K, D, dev, ksplit, rows, nt, cw, topk, out, no_pair);
     if (rc != KMASSIGN_OK)
         return rc;
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -409,6 +438,7 @@ AssignParams make_params(const Plan &plan, const float *cnorm, int32_t *idx, flo
     p.ntiles = plan.ntiles;
     p.num_units = plan.units;
     p.stages = plan.stages;
+    p.fold_stages = kma::pair_fold_stages(p.kblocks, plan.stages);
     p.xbufs = plan.xbufs;
     p.timeout_ns = g_wait_timeout_ns.load();
     return p;
@@ -708,18 +738,21 @@ extern "C" {
 int kmassign_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
                     float *sums, int32_t *counts, void *stream)
 {
+    DeviceRestore restore;
     return run_update(X, idx, N, K, D, sums, counts, 0, static_cast<cudaStream_t>(stream));
 }
 
 int kmassign_update_ex(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
                        float *sums, int32_t *counts, int method, void *stream)
 {
+    DeviceRestore restore;
     return run_update(X, idx, N, K, D, sums, counts, method, static_cast<cudaStream_t>(stream));
 }
 
 int kmassign_centroids(const float *sums, const int32_t *counts, const void *C_old, int64_t K,
                        int64_t D, void *C_new, float *means, void *stream)
 {
+    DeviceRestore restore;
     return run_centroids(sums, counts, C_old, K, D, C_new, means,
                          static_cast<cudaStream_t>(stream));
 }
@@ -727,6 +760,7 @@ int kmassign_centroids(const float *sums, const int32_t *counts, const void *C_o
 int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int iters,
                    int32_t *idx, void *stream)
 {
+    DeviceRestore restore;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int rc = check_shape(N, K, D);
     if (rc != KMASSIGN_OK)
@@ -853,20 +887,36 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
     DeviceInfo dev;
     if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
-    Plan plan;
-    if ((rc = make_plan(N, K, D, dev, 0, 0, 0, 0, false, &plan)) != KMASSIGN_OK)
-        return rc;
-    // A CTA pair that folds needs a fold operand this entry point has no room
-    // for: take the 256-row single-block shape instead.
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    // The automatic plan, unless it needs memory this entry point does not
+    // have: a CTA pair that folds the norms reads a fold operand from global
+    // memory (plan without CTA pairs instead), and a split centroid range
+    // over more points than the array's keys hold (plan without a split).
+    // Plans come from the same cache as kmassign's.
     const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
-    const bool no_pair = plan.v.pair && kma::assign_folds(plan.v, kblocks);
-    const int rows = no_pair ? 256 : 0, nt = no_pair ? 128 : 0;
-    if (no_pair && (rc = make_plan(N, K, D, dev, 0, rows, nt, 0, false, &plan)) != KMASSIGN_OK)
-        return rc;
-    // Keys for more points than the array holds: plan without a split.
-    if (plan.ksplit > 1 && N - split_first_row(plan) > kNoAllocKeyMax &&
-        (rc = make_plan(N, K, D, dev, 1, rows, nt, 0, false, &plan)) != KMASSIGN_OK)
-        return rc;
+    auto needs_operand = [&](const Plan &pl) {
+        return pl.v.pair && kma::assign_folds(pl.v, kblocks);
+    };
+    auto too_many_keys = [&](const Plan &pl) {
+        return pl.ksplit > 1 && N - split_first_row(pl) > kNoAllocKeyMax;
+    };
+    Plan plan;
+    int ksplit = 0;
+    bool no_pair = false;
+    for (int pass = 0; pass < 3; ++pass) {
+        if ((rc = cached_plan(N, K, D, dev, dev_id, ksplit, 0, 0, 0, &plan, false, no_pair)) !=
+            KMASSIGN_OK)
+            return rc;
+        if (needs_operand(plan))
+            no_pair = true;
+        else if (too_many_keys(plan))
+            ksplit = 1;
+        else
+            break;
+    }
+    if (needs_operand(plan) || too_many_keys(plan))
+        return KMASSIGN_ERR_ARG;   // unreachable: the last pass excludes both
 
     CUtensorMap xmap, cmap;
     if (!encode_map(&xmap, X, static_cast<uint64_t>(N), static_cast<uint64_t>(D), kma::kTileM) ||
@@ -912,12 +962,14 @@ extern "C" {
 int kmassign_noalloc(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
                      int64_t D, int32_t *idx, float *minscore, void *stream)
 {
+    DeviceRestore restore;
     return run_assign_noalloc(X, C, cnorm, N, K, D, idx, minscore,
                               static_cast<cudaStream_t>(stream));
 }
 
 int kmassign_norms(const void *C, int64_t K, int64_t D, float *cnorm, void *stream)
 {
+    DeviceRestore restore;
     int rc = check_shape(0, K, D);
     if (rc != KMASSIGN_OK)
         return rc;
@@ -936,6 +988,7 @@ int kmassign_norms(const void *C, int64_t K, int64_t D, float *cnorm, void *stre
 int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
              int32_t *idx, float *minscore, void *stream)
 {
+    DeviceRestore restore;
     return run_assign(X, C, cnorm, N, K, D, idx, minscore, 0, 0, 0, 0,
                       static_cast<cudaStream_t>(stream));
 }
@@ -944,6 +997,7 @@ int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int
                 int32_t *idx, float *minscore, int ksplit, int rows_per_cta,
                 int centroids_per_tile, int consumer_warps, void *stream)
 {
+    DeviceRestore restore;
     return run_assign(X, C, cnorm, N, K, D, idx, minscore, ksplit, rows_per_cta,
                       centroids_per_tile, consumer_warps, static_cast<cudaStream_t>(stream));
 }
@@ -952,6 +1006,7 @@ int kmassign_topk(const void *X, const void *C, const float *cnorm, int64_t N, i
                   int64_t D, int32_t k, int32_t *idx, float *score, int32_t distances,
                   void *stream)
 {
+    DeviceRestore restore;
     return run_topk(X, C, cnorm, N, K, D, k, idx, score, distances, 0,
                     static_cast<cudaStream_t>(stream));
 }
@@ -960,6 +1015,7 @@ int kmassign_topk_ex(const void *X, const void *C, const float *cnorm, int64_t N
                      int64_t D, int32_t k, int32_t *idx, float *score, int32_t distances,
                      int32_t ksplit, void *stream)
 {
+    DeviceRestore restore;
     return run_topk(X, C, cnorm, N, K, D, k, idx, score, distances, ksplit,
                     static_cast<cudaStream_t>(stream));
 }

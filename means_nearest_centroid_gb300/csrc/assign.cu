@@ -61,6 +61,8 @@
 // MMAs, and the tensor memory is freed before the block returns.
 #include "pipeline.cuh"
 
+#include <algorithm>
+
 namespace kma {
 namespace {
 
@@ -137,12 +139,13 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     constexpr int kNormWarp = kConsumerWarps + 2;
     constexpr int kXWarp = kConsumerWarps + 3;
     constexpr bool kSnap = KB <= 2;                    // D <= 128: epilogue-bound
-    // D <= 64: the norms enter the accumulator through one more MMA step
-    // (25% more tensor work at D = 64, a quarter of the reduction's
-    // instructions saved: measured 4-9% faster at D = 64 and 3-6% slower at
-    // D = 128, so only one k-block folds); the accumulator then holds
-    // t = x.c - ||c||^2 / 2 = -s / 2 and the reduction takes the largest t.
-    constexpr bool kFold = KB == 1;
+    // D <= 128: the norms enter the accumulator through one more MMA step
+    // (25% more tensor work at D = 64, 12.5% at D = 128); the accumulator then
+    // holds t = x.c - ||c||^2 / 2 = -s / 2, the reduction takes the largest t,
+    // and the tensor-memory loads reduce each chunk's maximum themselves.
+    // Every kernel folds at exactly these D, so a point's answer does not
+    // depend on the plan, the batch or the other points of the call.
+    constexpr bool kFold = KB <= 2;
     constexpr uint32_t kNormBytes =
         kFold ? kOnesBytes + kFoldStages * NT * 32u : kCnStages * NT * 4u;
     constexpr int kCW = NT / CH;                       // columns per consumer warp per tile
@@ -235,9 +238,16 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
                     for (int g = 0; g < kGroups; ++g) {
                         __syncwarp();   // tcgen05.ld is .sync.aligned
                         float v[kGroup][32];
+                        float m[kGroup];
 #pragma unroll
-                        for (int c = 0; c < kGroup; ++c)
-                            tmem_ld_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c]);
+                        for (int c = 0; c < kGroup; ++c) {
+                            // folded: the load also reduces the chunk's maximum
+                            if (kFold)
+                                tmem_ld_red_max_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c],
+                                                           m[c]);
+                            else
+                                tmem_ld_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c]);
+                        }
                         tmem_wait_ld();
                         if (g == kGroups - 1) {
                             // Scores are in registers: hand the stage back.
@@ -246,12 +256,9 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
                             if (lane == 0)
                                 mbar_arrive(bar(kBarAccEmpty + as));
                         }
-                        float m[kGroup];
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c) {
-                            if (kFold) {
-                                m[c] = chunk_max(v[c]);
-                            } else {
+                            if (!kFold) {
                                 apply_norms(v[c], cn_tile + 128u * (g * kGroup + c));
                                 m[c] = chunk_min(v[c]);
                             }
@@ -368,8 +375,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     // t = -s / 2.  Here the pair's N = 256 MMAs leave the tensor pipe room
     // for the extra step, and the lighter reduction is what sets the pace.
     constexpr bool kFold = KB <= 2;
-    constexpr uint32_t kNormBytes =
-        kFold ? kOnesBytes + kFoldStages * kFoldBlockBytes : kCnStages * NT * 4u;
     constexpr int kCW = NT / CH;
     constexpr int kChunks = kCW / 32;
     constexpr int kGroup = kChunks < 4 ? kChunks : 4;
@@ -388,7 +393,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     const uint32_t x_base = base;
     const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
     const uint32_t cn_base = c_base + p.stages * kCStageBytes;
-    const uint32_t red_base = cn_base + kNormBytes;   // fold: ones tile, then fold slots
+    // fold: the ones tile, then p.fold_stages fold slots; else the norm ring
+    const uint32_t norm_bytes =
+        kFold ? kOnesBytes + static_cast<uint32_t>(p.fold_stages) * kFoldBlockBytes
+              : kCnStages * NT * 4u;
+    const uint32_t red_base = cn_base + norm_bytes;
     const uint32_t snap_base = red_base + (CH - 1) * kTileM * 8;
     const uint32_t bar_base = snap_base + (kSnap ? kConsumerWarps * 4096u : 0u);
     uint8_t *const sbase = smem_raw + (base - raw);
@@ -419,11 +428,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
             mbar_init(bar(kBarCEmpty + s), 1);
         }
         for (int s = 0; s < kCnStages; ++s) {
-            // folded: the fold slots' full barriers count the leader's
-            // expect_tx and both CTAs' copied bytes; the pair MMA's commit
-            // frees a slot in both CTAs
-            mbar_init(bar(kBarCnFull + s), kFold ? 1 : 32);
-            mbar_init(bar(kBarCnEmpty + s), kFold ? 1 : kConsumerWarps);
+            mbar_init(bar(kBarCnFull + s), 32);
+            mbar_init(bar(kBarCnEmpty + s), kConsumerWarps);
+        }
+        for (int s = 0; s < kMaxStages; ++s) {
+            // the fold slots' full barriers count the leader's expect_tx and
+            // both CTAs' copied bytes; the pair MMA's commit frees a slot in
+            // both CTAs
+            mbar_init(bar(kBarFoldFull + s), 1);
+            mbar_init(bar(kBarFoldEmpty + s), 1);
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -471,15 +484,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                     if (kFold && ok) {
                         // this CTA's 128 centroids of the tile: fold block
                         // 2 * tile + rank, 256 rows of 16 bytes
-                        const uint32_t fs = fold_n % kFoldStages;
-                        const uint32_t fph = (fold_n / kFoldStages) & 1u;
-                        if (!(ok = wait1(bar(kBarCnEmpty + fs), fph ^ 1u, abort_flag,
+                        const uint32_t fs = fold_n % static_cast<uint32_t>(p.fold_stages);
+                        const uint32_t fph = (fold_n / static_cast<uint32_t>(p.fold_stages)) & 1u;
+                        if (!(ok = wait1(bar(kBarFoldEmpty + fs), fph ^ 1u, abort_flag,
                                          p.timeout_ns)))
                             break;
                         if (leader)
-                            mbar_arrive_expect_tx(bar(kBarCnFull + fs), 2 * kFoldBlockBytes);
+                            mbar_arrive_expect_tx(bar(kBarFoldFull + fs), 2 * kFoldBlockBytes);
                         tma_load_2d_pair(cn_base + kOnesBytes + fs * kFoldBlockBytes, &fmap,
-                                         lead_bar(kBarCnFull + fs), 0,
+                                         lead_bar(kBarFoldFull + fs), 0,
                                          (2 * tile + static_cast<int>(rank)) * 256, pol_c);
                         ++fold_n;
                     }
@@ -574,9 +587,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                     if (!ok)
                         break;
                     if (kFold) {
-                        const uint32_t fb = fold_used % kFoldStages;
-                        const uint32_t fph = (fold_used / kFoldStages) & 1u;
-                        if (!(ok = wait_warp(bar(kBarCnFull + fb), fph, abort_flag,
+                        const uint32_t fb = fold_used % static_cast<uint32_t>(p.fold_stages);
+                        const uint32_t fph =
+                            (fold_used / static_cast<uint32_t>(p.fold_stages)) & 1u;
+                        if (!(ok = wait_warp(bar(kBarFoldFull + fb), fph, abort_flag,
                                              p.timeout_ns)))
                             break;
                         const uint64_t bdesc =
@@ -584,7 +598,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                                               kFoldPairLbo, kFoldPairSbo);
                         if (elect_one()) {
                             mma_bf16_pair(d_tmem, ones_desc, bdesc, kIdesc, 1u);
-                            mma_commit_pair(bar(kBarCnEmpty + fb), kBoth);
+                            mma_commit_pair(bar(kBarFoldEmpty + fb), kBoth);
                         }
                         __syncwarp();
                         ++fold_used;
@@ -664,9 +678,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                     for (int g = 0; g < kGroups; ++g) {
                         __syncwarp();
                         float v[kGroup][32];
+                        float m[kGroup];
 #pragma unroll
-                        for (int c = 0; c < kGroup; ++c)
-                            tmem_ld_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c]);
+                        for (int c = 0; c < kGroup; ++c) {
+                            // folded: the load also reduces the chunk's maximum
+                            if (kFold)
+                                tmem_ld_red_max_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c],
+                                                           m[c]);
+                            else
+                                tmem_ld_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c]);
+                        }
                         tmem_wait_ld();
                         if (g == kGroups - 1) {
                             tc_fence_before();
@@ -678,12 +699,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                                     mbar_arrive_cluster(lead_bar(kBarAccEmpty + as));
                             }
                         }
-                        float m[kGroup];
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c) {
-                            if (kFold) {
-                                m[c] = chunk_max(v[c]);
-                            } else {
+                            if (!kFold) {
                                 apply_norms(v[c], cn_tile + 128u * (g * kGroup + c));
                                 m[c] = chunk_min(v[c]);
                             }
@@ -883,13 +901,19 @@ const Variant kVariants[kNumVariants] = {{2, 128, 1, false}, {1, 256, 2, false},
                                          {1, 256, 4, false}, {1, 256, 2, true},
                                          {1, 256, 4, true}};
 
+int pair_fold_stages(int kblocks, int stages)
+{
+    return std::min(kMaxStages, std::max(2, (stages + kblocks - 1) / kblocks));
+}
+
 size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 {
     const size_t stage_rows = v.pair ? v.nt / 2 : v.nt;
     const bool fold = assign_folds(v, kblocks);   // the kernels' kFold
+    const size_t fold_slots = v.pair ? pair_fold_stages(kblocks, stages) : kFoldStages;
     const size_t fold_slot = v.pair ? kFoldBlockBytes : static_cast<size_t>(v.nt) * 32;
     const size_t norm_bytes =
-        fold ? kOnesBytes + static_cast<size_t>(kFoldStages) * fold_slot : kCnStages * v.nt * 4;
+        fold ? kOnesBytes + fold_slots * fold_slot : kCnStages * v.nt * 4;
     return 1024 + static_cast<size_t>(xbufs) * v.sub * kblocks * kXTileBytes +
            static_cast<size_t>(stages) * stage_rows * 128 + norm_bytes +
            static_cast<size_t>(v.ch - 1) * v.sub * kTileM * 8 +
@@ -942,9 +966,9 @@ cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int 
     return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
 }
 
-bool assign_folds(const Variant &v, int kblocks)
+bool assign_folds(const Variant &, int kblocks)
 {
-    return v.pair ? kblocks <= 2 : kblocks == 1;
+    return kblocks <= 2;
 }
 
 int64_t fold_operand_blocks(int64_t K)

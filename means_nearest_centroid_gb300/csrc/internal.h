@@ -37,6 +37,7 @@ struct AssignParams {
     int32_t ntiles;                // ceil(K / nt)
     int32_t num_units;             // full_units + (rowtiles - split_row0) * ksplit
     int32_t stages;                // shared-memory ring depth
+    int32_t fold_stages;           // CTA pair folding the norms: fold-operand ring depth
     int32_t xbufs;                 // X tile buffers (1 or 2)
     uint64_t timeout_ns;           // bound on every pipeline wait
 };
@@ -62,13 +63,16 @@ cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
                           const CUtensorMap &xmap, const CUtensorMap &cmap,
                           const CUtensorMap &fmap, int grid, size_t smem_bytes,
                           cudaStream_t stream);
-// Whether the shape's kernel folds the norms into the MMA (single-block
-// kernels at one k-block, CTA pairs at up to two).
+// Whether the shape's kernel folds the norms into the MMA (every shape at up
+// to two k-blocks, D <= 128).
 bool assign_folds(const Variant &v, int kblocks);
 // The CTA pair's fold operand: fold_operand_blocks(K) blocks of 128
 // centroids, 4 KiB each ([K half][128 rows][16 B] bf16), written from the
 // norms by launch_fold_operand (rows past K hold NaN).
 int64_t fold_operand_blocks(int64_t K);
+// Fold-operand slots of a folding CTA pair with `stages` C stages: one per
+// tile the C ring holds (at least 2, at most kMaxStages).
+int pair_fold_stages(int kblocks, int stages);
 size_t fold_operand_bytes(int64_t K);
 cudaError_t launch_fold_operand(const float *cnorm, int64_t K, void *out, cudaStream_t stream);
 

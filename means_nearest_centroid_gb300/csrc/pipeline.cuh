@@ -38,12 +38,14 @@ constexpr int kBarCEmpty = kBarCFull + kMaxStages;    // [kMaxStages]
 constexpr int kCnStages = 4;                          // centroid-norm ring depth
 constexpr int kBarCnFull = kBarCEmpty + kMaxStages;   // [kCnStages]
 constexpr int kBarCnEmpty = kBarCnFull + kCnStages;   // [kCnStages]
-constexpr int kNumBars = kBarCnEmpty + kCnStages;
+constexpr int kBarFoldFull = kBarCnEmpty + kCnStages; // [kMaxStages] CTA pair's fold ring
+constexpr int kBarFoldEmpty = kBarFoldFull + kMaxStages;   // [kMaxStages]
+constexpr int kNumBars = kBarFoldEmpty + kMaxStages;
 constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot + abort flag
-// Norm folding (single-block kernels at D <= 64, CTA pairs at D <= 128): the
-// norms enter the accumulator through one more K = 16 MMA step per tile,
-// A = a constant tile of ones, B = the tile's -||c||^2 / 2 split into three
-// bf16 parts.  Single-block shared memory: the ones tile, then kFoldStages
+// Norm folding (every assignment kernel at D <= 128, the k-nearest kernel at
+// every D): the norms enter the accumulator through one more K = 16 MMA step
+// per tile, A = a constant tile of ones, B = the tile's -||c||^2 / 2 split
+// into three bf16 parts.  Single-block shared memory: the ones tile, then kFoldStages
 // slots of NT rows x 32 bytes (plain K-major layout: 8-row groups of 256
 // bytes, each two 128-byte core matrices along K) that a norm warp fills.
 constexpr int kFoldStages = 3;
@@ -52,7 +54,10 @@ constexpr uint32_t kFoldLbo = 128;                    // between the two core ma
 constexpr uint32_t kFoldSbo = 256;                    // between 8-row groups
 // The CTA pair's fold operand comes from global memory by TMA, one block of
 // 128 centroids (4 KiB) per CTA and tile, laid out [K half][128 rows][16 B]:
-// the same unswizzled K-major core matrices with other offsets.
+// the same unswizzled K-major core matrices with other offsets.  Its ring has
+// a slot per tile the C ring can hold (pair_fold_stages), so the producer,
+// which loads a tile's C k-blocks and then its fold block, never waits for a
+// fold slot before the C ring is full.
 constexpr uint32_t kFoldBlockBytes = 4096;
 constexpr uint32_t kFoldPairLbo = 2048;               // between the two K halves
 constexpr uint32_t kFoldPairSbo = 128;                // between 8-row groups
@@ -170,22 +175,6 @@ __device__ __forceinline__ float chunk_min(const float (&s)[32])
     const float b2 = min3(a[6], a[7], a[8]);
     const float b3 = min2(a[9], a[10]);
     return min3(b0, b1, min2(b2, b3));
-}
-
-// Maximum of 32 values by a tree of 3-input maxes (a NaN is ignored unless
-// every value is NaN).
-__device__ __forceinline__ float chunk_max(const float (&s)[32])
-{
-    float a[11];
-#pragma unroll
-    for (int i = 0; i < 10; ++i)
-        a[i] = max3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-    a[10] = max2(s[30], s[31]);
-    const float b0 = max3(a[0], a[1], a[2]);
-    const float b1 = max3(a[3], a[4], a[5]);
-    const float b2 = max3(a[6], a[7], a[8]);
-    const float b3 = max2(a[9], a[10]);
-    return max3(b0, b1, max2(b2, b3));
 }
 
 // s[i] = fmaf(-2, acc[i], cnorm[j0 + i]) in place, norms from shared memory.

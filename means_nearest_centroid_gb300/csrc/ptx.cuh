@@ -212,6 +212,33 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[32
         v[i] = __uint_as_float(r[i]);
 }
 
+// The same load, and the largest of the thread's 32 values in `mx`, reduced
+// by the tensor-memory load path itself (sm_103a).  Measured on GB300: the
+// values equal the plain load's; mx ignores NaN unless all 32 are NaN (then
+// NaN), keeps subnormals, orders -inf < finite < +inf, and gives +0 for a mix
+// of +0 and -0 -- the result of a tree of max.f32 over the 32 values, up to
+// the sign of a zero.  Valid, like the values, after tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld_red_max_32x32b_x32(uint32_t taddr, float (&v)[32],
+                                                            float &mx)
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31]), "=f"(mx)
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
 // ---------------------------------------------------- CTA pairs (clusters of 2)
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {

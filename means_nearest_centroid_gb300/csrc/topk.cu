@@ -268,9 +268,10 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
                     for (int g = 0; g < kGroups; ++g) {
                         __syncwarp();   // tcgen05.ld is .sync.aligned
                         float v[kGroup][32];
+                        float m[kGroup];   // chunk maxima, reduced by the loads
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c)
-                            tmem_ld_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c]);
+                            tmem_ld_red_max_32x32b_x32(taddr + (g * kGroup + c) * 32, v[c], m[c]);
                         tmem_wait_ld();
                         if (g == kGroups - 1) {
                             // Scores are in registers: hand the stage back.
@@ -279,10 +280,6 @@ __global__ void __launch_bounds__(32 * (kTopConsumerWarps + 4), 1)
                             if (lane == 0)
                                 mbar_arrive(bar(kBarAccEmpty + as));
                         }
-                        float m[kGroup];
-#pragma unroll
-                        for (int c = 0; c < kGroup; ++c)
-                            m[c] = chunk_max(v[c]);
                         const int jg = tile * NT + g * kGroup * 32;
 #pragma unroll
                         for (int c = 0; c < kGroup; ++c)

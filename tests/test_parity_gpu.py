@@ -1,6 +1,9 @@
 """CUDA path vs the fp64 oracle, through the C ABI (needs a GB300)."""
 
+import json
 import math
+import os
+import time
 
 import numpy as np
 import pytest
@@ -37,18 +40,6 @@ def is_pair(plan):
 def plans_for(D):
     """The plans a shape can run: every compiled shape, at every D."""
     return list(PLANS)
-
-
-def folds(plan, N, K, D):
-    """Whether the plan's kernel folds the norms into the MMA (every kernel at
-    D <= 64, the CTA pair up to D = 128).  Plans of one class give identical
-    bits (the single-block and pair folds included); across classes the
-    accumulators round differently (both within the tolerance) on float data,
-    and agree exactly on integer data."""
-    if D <= 64:
-        return True
-    p = km.kmassign_plan(N, K, D, **plan)
-    return D <= 128 and p["rows_per_cta"] == 256 and p["centroids_per_tile"] == 256
 
 
 @pytest.fixture(scope="module")
@@ -167,38 +158,48 @@ def test_adversarial_specials_every_plan_wider_rows(dev, D):
         assert torch.equal(ms.view(torch.int32), ref[1].view(torch.int32)), plan
 
 
-def test_plans_give_identical_bits_on_float_data(dev):
-    """D = 128: the single-block plans agree bit for bit, and so do the
-    folding CTA-pair plans; both classes pass the oracle."""
-    N, K, D = 1500, 1300, 128
-    X, C = workloads.iid(N, K, D, seed=99)
-    refs = {}
-    classes = set()
+@pytest.mark.parametrize("D", [16, 48, 64, 96, 128, 192, 256])
+def test_plans_give_identical_bits_on_float_data(dev, D):
+    """Every plan (every tile shape, warp count and split, the CTA pairs
+    included) returns the same idx and minscore bits on float data: at
+    D <= 128 every kernel folds the norms into the MMA, above it none does, so
+    a point's arithmetic does not depend on the plan.  The first plan is also
+    checked against the oracle."""
+    N, K = 1500, 1300
+    X, C = workloads.iid(N, K, D, seed=99 + D)
+    ref = None
     for plan in plans_for(D):
         idx, ms = run(dev, X, C, plan=plan)
-        rep = parity.compare(X, C, idx, ms)
-        assert rep.ok(), (plan, rep)
-        cls = folds(plan, N, K, D)
-        classes.add(cls)
-        if cls not in refs:
-            refs[cls] = (idx, ms)
-            continue
-        assert torch.equal(idx, refs[cls][0]), plan
-        assert torch.equal(ms.view(torch.int32), refs[cls][1].view(torch.int32)), plan
-    assert classes == {False, True}
-
-
-def test_plans_give_identical_bits_on_float_data_with_pairs(dev):
-    """D = 256: the CTA-pair kernel (not folding here) joins the comparison."""
-    X, C = workloads.iid(1500, 1300, 256, seed=98)
-    ref = None
-    for plan in plans_for(256):
-        idx, ms = run(dev, X, C, plan=plan)
         if ref is None:
+            rep = parity.compare(X, C, idx, ms)
+            assert rep.ok(), (plan, rep)
             ref = (idx, ms)
             continue
         assert torch.equal(idx, ref[0]), plan
         assert torch.equal(ms.view(torch.int32), ref[1].view(torch.int32)), plan
+
+
+@pytest.mark.parametrize("D", [64, 96, 128, 192, 256])
+def test_answers_do_not_depend_on_the_batch(dev, D):
+    """A point's idx and minscore bits are the same whether it is assigned
+    alone, in a slice of the rows or with all of them, although the planner
+    picks different shapes and splits for the different N (at D = 96 and 128
+    the whole batch runs on CTA pairs, the small slices on single blocks)."""
+    N, K = 70000, 4096
+    X, C = workloads.iid(N, K, D, seed=7 * D)
+    Xd, Cd = X.to(dev), C.to(dev)
+    cn = km.kmassign_norms(Cd)
+    ms = torch.empty(N, dtype=torch.float32, device=dev)
+    idx = km.kmassign(Xd, Cd, cnorm=cn, minscore=ms)
+    plans = {str(km.kmassign_plan(N, K, D))}
+    for a, b in [(0, 1), (5, 300), (1000, 9000), (40000, 70000), (123, 65659)]:
+        ms_s = torch.empty(b - a, dtype=torch.float32, device=dev)
+        idx_s = km.kmassign(Xd[a:b].contiguous(), Cd, cnorm=cn, minscore=ms_s)
+        plans.add(str(km.kmassign_plan(b - a, K, D)))
+        assert torch.equal(idx_s, idx[a:b]), (a, b)
+        assert torch.equal(ms_s.view(torch.int32), ms[a:b].view(torch.int32)), (a, b)
+    assert km.kmassign_check() == 0
+    assert len(plans) >= 2
 
 
 def test_repeat_runs_are_bitwise_identical(dev):
@@ -247,6 +248,20 @@ def test_assign_host_chunked_matches_device_call(dev, N, chunks):
     assert torch.equal(got, ref)
 
 
+@pytest.mark.parametrize("D,K", [(96, 16384), (128, 4096), (128, 16384)])
+def test_assign_host_slices_match_whole_call_folding_pairs(dev, D, K):
+    """At D = 96 and 128, where the whole call runs on CTA pairs and the
+    slices of the host path on other shapes, the slices still give the whole
+    call's bits."""
+    N = 90000
+    X, C = workloads.iid(N, K, D, seed=D + K)
+    plan = km.kmassign_plan(N, K, D)
+    assert (plan["rows_per_cta"], plan["centroids_per_tile"]) == (256, 256), plan
+    got = km.assign_host(X.pin_memory(), C.pin_memory(), chunks=7)
+    ref = km.kmassign(X.to(dev), C.to(dev)).cpu()
+    assert torch.equal(got, ref)
+
+
 def test_assign_host_short_first_slice(dev):
     X, C = workloads.blobs(4000, 300, 64, seed=40)
     got = km.assign_host(X.pin_memory(), C.pin_memory(), chunks=5, first_rows=37)
@@ -276,12 +291,21 @@ def test_many_centroids(dev):
 
 
 # ---------------------------------------------------------------- full sizes
-FULL_SAMPLE = {"tiny_blobs": None, "sampled_centroids": 8192, "iid_normal": 2048,
-               "lognormal_clusters": 4096, "adversarial_ties": None}
+def _record(entry):
+    """Append one JSON line to the file named by KMASSIGN_PARITY_REPORT, if set."""
+    path = os.environ.get("KMASSIGN_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(entry) + "\n")
 
 
 @pytest.mark.parametrize("key", workloads.ORDER)
 def test_full_size_workloads(dev, key):
+    """Every row of each of the five workloads, at full size, against the
+    oracle: bit-exact idx and minscore on integer data, the tolerance rule on
+    float data.  The number of rows whose idx differs from the oracle's (each
+    within the tolerance) and the largest accepted gap are printed and, with
+    KMASSIGN_PARITY_REPORT set, appended to that file."""
     w = workloads.WORKLOADS[key]
     X, C = workloads.make(key)
     Xd, Cd = X.to(dev), C.to(dev)
@@ -289,16 +313,18 @@ def test_full_size_workloads(dev, key):
     ms = torch.empty(w.N, dtype=torch.float32, device=dev)
     idx = km.kmassign(Xd, Cd, cnorm=cn, minscore=ms)
     assert km.kmassign_check() == 0
+    plan = km.kmassign_plan(w.N, w.K, w.D)
     idx, ms = idx.cpu(), ms.cpu()
-    n = FULL_SAMPLE[key]
-    if n is None:
-        rows = None
-    else:
-        g = np.random.default_rng(w.seed)
-        rows = np.unique(np.concatenate([g.choice(w.N, n, replace=False),
-                                         [0, w.N - 1], np.arange(w.N - 300, w.N)]))
-    rep = parity.compare(X, C, idx, ms, rows=rows, integer=w.integer)
-    print(key, rep)
+    t0 = time.time()
+    rep = parity.compare(X, C, idx, ms, rows=None, integer=w.integer)
+    entry = dict(workload=key, N=w.N, K=w.K, D=w.D, rows=rep.rows,
+                 idx_mismatches=rep.idx_mismatches, rejected=rep.rejected,
+                 minscore_bad=rep.minscore_bad, worst_gap=rep.worst_gap,
+                 integer=bool(w.integer), oracle_s=round(time.time() - t0, 1),
+                 plan=plan)
+    print(entry)
+    _record(entry)
+    assert rep.rows == w.N
     assert rep.ok(), rep
     if w.integer:
         assert rep.idx_mismatches == 0
