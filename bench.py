@@ -1,8 +1,9 @@
 """Benchmark of the k-means assignment step on GB300 (one JSON line).
 
 A step is one pass of the whole hot path over one batch of synthetic input:
-centroid norms (kmassign_norms) + assignment (kmassign), inputs resident in
-HBM.  Default workload: N=262,144 points, D=256, K=16,384 centroids, X and C
+centroid norms + assignment (one kmassign call with cnorm NULL, which forms
+the norms inside; kmassign_norms ahead of the timing for the workload whose
+norms are precomputed), inputs resident in HBM.  Default workload: N=262,144 points, D=256, K=16,384 centroids, X and C
 iid N(0,1) in bf16 -- the shape the throughput target is stated on.
 
 Metric: TFLOP/s counted as 2*N*K*D per step (the dense X.C^T the method
@@ -202,6 +203,70 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(s["sm"] for s in inside),
                 "sm_max_mhz": max(s["smax"] for s in inside),
                 "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+class NvmlClockSampler:
+    """The SM clock and the clock-event reasons read in-process through NVML
+    (query calls only; nothing is set), every ~0.25 ms while running, so that
+    even a timed region of a few tens of milliseconds gets many samples."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            uuid = str(getattr(torch.cuda.get_device_properties(device_index), "uuid", ""))
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) != 0:
+                return
+            self.lib, self.handle, self.ct = lib, handle, ctypes
+            clk = ctypes.c_uint()
+            if lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) != 0:   # 1: SM clock
+                return
+            mx = ctypes.c_uint()
+            self.max_mhz = (float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(
+                handle, 1, ctypes.byref(mx)) == 0 else None)
+        except (OSError, AttributeError):
+            return
+        self.ok = True
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _run(self):
+        ct, lib, h = self.ct, self.lib, self.handle
+        clk = ct.c_uint()
+        rs = ct.c_ulonglong()
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0:
+                r = (rs.value if lib.nvmlDeviceGetCurrentClocksEventReasons(h, ct.byref(rs)) == 0
+                     else 0)
+                self.samples.append((time.time(), float(clk.value), int(r)))
+            time.sleep(0.00025)
+
+    def stop(self):
+        self._stop.set()
+        if self.ok:
+            self.thread.join(timeout=5)
+            self.lib.nvmlShutdown()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return None
+        reasons = sorted({name for _, _, r in inside for bit, name in self.REASONS.items()
+                          if r & bit})
+        mhz = [m for _, m, _ in inside]
+        return {"sm_mhz": statistics.median(mhz), "sm_mhz_min": min(mhz), "sm_mhz_max": max(mhz),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(inside),
+                "source": "NVML in-process, every ~0.25 ms over the timed steps"}
 
 
 def make_inputs(key, variants, device, N=None, K=None, D=None):
@@ -550,20 +615,22 @@ def main():
     flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=device) if flush else None
 
     def step(i, ev_mid=None, ev_end=None, ev_begin=None):
+        # norms in the step: one call with cnorm NULL, which computes them
+        # inside (in the same launch that prepares the call's other inputs)
         X, C = dsets[i % 3]
         if flush_buf is not None:
             flush_buf.fill_(i & 0xff)
         if ev_begin is not None:
             ev_begin.record(stream)
-        if norms_in_step:
-            km.kmassign_norms(C, out=cns[i % 3], stream=stream)
         if ev_mid is not None:
             ev_mid.record(stream)
-        km.kmassign(X, C, cnorm=cns[i % 3], idx=idxs[i % 3], stream=stream)
+        km.kmassign(X, C, cnorm=None if norms_in_step else cns[i % 3], idx=idxs[i % 3],
+                    stream=stream)
         if ev_end is not None:
             ev_end.record(stream)
 
     sampler = ClockSampler(local)
+    nvml = NvmlClockSampler(local)
     time.sleep(0.3)
     for i in range(args.warmup):
         step(i)
@@ -593,6 +660,7 @@ def main():
     if rc != 0:
         raise SystemExit(f"timed run failed: {km.kmassign_strerror(rc)}")
     sampler.stop()
+    nvml.stop()
     total_ms = t_start.elapsed_time(t_stop)
     kern_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
     if flush_buf is not None:
@@ -621,6 +689,8 @@ def main():
                 "peak_source": f"{peak_src} bf16 dense (burst)",
                 "kernel": ("assign_pair_kernel (tcgen05.cta_group::2, " if pair
                            else "assign_kernel (tcgen05, ") + tile + " tiles)",
+                "timed": "the kmassign call around the kernel (its preparation launch, when "
+                         "one runs, included), CUDA events on the launching stream",
                 "kernel_ms_avg": kernel_avg_ms,
                 "kernel_ms_median": kernel_med_ms,
                 "algorithmic_bytes": N * D * 2 + K * D * 2 + N * 4 + K * 4}
@@ -679,11 +749,23 @@ def main():
                          f"{secs:.1f} s, fp64 oracle (OpenMP over points)"}
 
     clocks = sampler.summary(wall0, wall1)
-    # norms (when computed in the step), the fold operand (a CTA pair that
-    # folds the norms: D <= 128), the assignment, and the split rows' finalize
+    nv = nvml.summary(wall0, wall1)
+    if nv is not None and nv["samples"] >= 5:
+        smi = clocks
+        clocks = dict(nv)
+        clocks["reasons"] = sorted(set(nv["reasons"]) | set(smi.get("reasons", [])))
+        clocks["nvidia_smi"] = smi
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    if clocks.get("sm_mhz"):
+        # clock-normalised rate of the dominant kernel: flop per SM clock
+        roofline["flop_per_clk_per_sm"] = achieved * 1e12 / (sms * clocks["sm_mhz"] * 1e6)
+        roofline["sms"] = sms
+    # the preparation launch (norms when computed in the step, the fold
+    # operand of a CTA pair folding the norms at D <= 128, the split rows'
+    # keys) and the assignment kernel, which also finalizes split rows
     folding_pair = pair and D <= 128
-    launches_per_step = ((1 if norms_in_step else 0) + (1 if folding_pair else 0) + 1 +
-                         (1 if plan["ksplit"] > 1 else 0))
+    prep = norms_in_step or folding_pair or plan["ksplit"] > 1
+    launches_per_step = (1 if prep else 0) + 1
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

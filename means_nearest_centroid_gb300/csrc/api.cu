@@ -226,11 +226,13 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 //     tile with 4 warps;
 //   * a CTA pair costs its measured tile time: above D = 128 the larger of
 //     its MMA time and floor, scaled by 0.94; at D <= 128, where it folds,
-//     ~1390 (D = 64) / ~1420 (D = 128) clocks with 8 warps, plus ~6000
-//     clocks per call for the fold operand;
+//     ~1390 (D = 64) / ~1420 (D = 128) clocks with 8 warps, plus ~4000
+//     clocks per call for the fold operand (written by the preparation
+//     launch, which computes the norms too when the caller gives none);
 //   * a unit pays ~5000 clocks to load its X tile and fill the pipe;
-//   * any split pays ~12000 clocks for the key memset, the finalize kernel
-//     and their launches.
+//   * any split pays ~5000 clocks: the keys' initial values (the same
+//     preparation launch) and the arrival count at the end of each split
+//     unit, whose last unit turns the keys into the answers.
 // Splits considered: every row tile into ks centroid ranges (ks >= 1), or
 // only the row tiles of the last partial wave (the rest stay whole), which
 // evens out the last wave when there are a few waves of whole row tiles.
@@ -306,7 +308,7 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const bool pair_fold = v.pair && fold;
         const double tile = pair_fold ? (v.ch == 2 ? (kblocks == 1 ? 1390.0 : 1420.0) : 1600.0)
                                       : std::max(tile_mma, tile_epi) * (v.pair ? pair_factor : 1.0);
-        const double call_over = pair_fold ? 6000.0 : 0.0;
+        const double call_over = pair_fold ? 4000.0 : 0.0;
         const double unit_over = 5000.0;
 
         // Candidate (F whole row tiles, split the rest into ks ranges).
@@ -334,7 +336,7 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
                                  double(ns) * (double(chunk) * tile + unit_over);
                 worst = std::max(worst, c);
             }
-            const double cost = worst + (any_split ? 12000.0 : 0.0) + call_over;
+            const double cost = worst + (any_split ? 5000.0 : 0.0) + call_over;
             if (!found || cost < best_cost * 0.995) {
                 found = true;
                 best_cost = cost;
@@ -495,55 +497,46 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
                     c_box_rows(plan)))
         return KMASSIGN_ERR_CUDA;
 
+    // Temporaries from the pool, all filled by one preparation launch: the
+    // norms (when not given), the fold operand of a CTA pair that folds the
+    // norms, and the split rows' packed keys and arrival counters.
     float *tmp_norm = nullptr;
-    unsigned long long *keys = nullptr;
-    rc = KMASSIGN_OK;
-    if (cnorm == nullptr) {
-        if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&tmp_norm),
-                                    static_cast<size_t>(K) * 4, dev.pool, stream) != cudaSuccess)
-            return KMASSIGN_ERR_CUDA;
-        if (kma::launch_norms(C, K, D, tmp_norm, stream) != cudaSuccess)
-            rc = KMASSIGN_ERR_CUDA;
-        cnorm = tmp_norm;
-    }
+    void *fold = nullptr;
+    unsigned char *split = nullptr;
+    const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
+    const bool need_fold = plan.v.pair && kma::assign_folds(plan.v, kblocks);
     const int64_t row_split = split_first_row(plan);
     const int64_t n_split = plan.ksplit > 1 ? N - row_split : 0;
-    if (rc == KMASSIGN_OK && n_split > 0) {
-        if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&keys),
-                                    static_cast<size_t>(n_split) * 8, dev.pool,
-                                    stream) != cudaSuccess ||
-            cudaMemsetAsync(keys, 0xff, static_cast<size_t>(n_split) * 8, stream) != cudaSuccess)
-            rc = KMASSIGN_ERR_CUDA;
-    }
-    // A CTA pair that folds the norms reads them as a fold operand.
-    void *fold = nullptr;
+    const size_t split_bytes = n_split > 0 ? kma::split_scratch_bytes(n_split) : 0;
+    auto take = [&](void **ptr, size_t bytes) {
+        return cudaMallocFromPoolAsync(ptr, bytes, dev.pool, stream) == cudaSuccess;
+    };
+    rc = KMASSIGN_OK;
+    if ((cnorm == nullptr &&
+         !take(reinterpret_cast<void **>(&tmp_norm), static_cast<size_t>(K) * 4)) ||
+        (need_fold && !take(&fold, kma::fold_operand_bytes(K))) ||
+        (split_bytes > 0 && !take(reinterpret_cast<void **>(&split), split_bytes)))
+        rc = KMASSIGN_ERR_CUDA;
     CUtensorMap fmap{};
-    const int kblocks = static_cast<int>(cdiv(D, kma::kKBlock));
-    if (rc == KMASSIGN_OK && plan.v.pair && kma::assign_folds(plan.v, kblocks)) {
-        if (cudaMallocFromPoolAsync(&fold,
-                                    kma::fold_operand_bytes(K), dev.pool, stream) != cudaSuccess)
-            rc = KMASSIGN_ERR_CUDA;
-        else if (kma::launch_fold_operand(cnorm, K, fold, stream) != cudaSuccess ||
-                 !encode_fold_map(&fmap, fold, K))
+    if (rc == KMASSIGN_OK && (tmp_norm != nullptr || fold != nullptr || split != nullptr)) {
+        if (kma::launch_prep(C, K, D, cnorm, tmp_norm, fold, split, split_bytes, stream) !=
+                cudaSuccess ||
+            (fold != nullptr && !encode_fold_map(&fmap, fold, K)))
             rc = KMASSIGN_ERR_CUDA;
     }
     if (rc == KMASSIGN_OK) {
-        const AssignParams p = make_params(plan, cnorm, idx, minscore, keys, N, K, D);
+        AssignParams p = make_params(plan, cnorm != nullptr ? cnorm : tmp_norm, idx, minscore,
+                                     reinterpret_cast<unsigned long long *>(split), N, K, D);
+        if (split != nullptr)
+            p.counters =
+                reinterpret_cast<uint32_t *>(split + kma::split_counter_offset(n_split));
         if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, fmap, plan.grid, plan.smem,
                                stream) != cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
-        else if (keys != nullptr &&
-                 kma::launch_finalize(keys, n_split, idx + row_split,
-                                      minscore ? minscore + row_split : nullptr,
-                                      stream) != cudaSuccess)
-            rc = KMASSIGN_ERR_CUDA;
     }
-    if (fold != nullptr && cudaFreeAsync(fold, stream) != cudaSuccess)
-        rc = KMASSIGN_ERR_CUDA;
-    if (keys != nullptr && cudaFreeAsync(keys, stream) != cudaSuccess)
-        rc = KMASSIGN_ERR_CUDA;
-    if (tmp_norm != nullptr && cudaFreeAsync(tmp_norm, stream) != cudaSuccess)
-        rc = KMASSIGN_ERR_CUDA;
+    for (void *t : {static_cast<void *>(split), fold, static_cast<void *>(tmp_norm)})
+        if (t != nullptr && cudaFreeAsync(t, stream) != cudaSuccess)
+            rc = KMASSIGN_ERR_CUDA;
     return rc;
 }
 
@@ -837,7 +830,9 @@ int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int 
 constexpr int64_t kNoAllocNormMax = int64_t(1) << 20;   // K, when cnorm is NULL
 constexpr int64_t kNoAllocKeyMax = int64_t(1) << 18;    // N, for a split centroid range
 constexpr size_t kNoAllocNormBytes = static_cast<size_t>(kNoAllocNormMax) * 4;
-constexpr size_t kNoAllocBytes = kNoAllocNormBytes + static_cast<size_t>(kNoAllocKeyMax) * 8;
+// the keys and, after them, one arrival counter per 128 split points
+constexpr size_t kNoAllocBytes =
+    kNoAllocNormBytes + static_cast<size_t>(kNoAllocKeyMax) * 8 + kNoAllocKeyMax / 128 * 4;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
@@ -927,30 +922,25 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
     unsigned char *scratch = nullptr;
     if ((rc = noalloc_scratch(&scratch)) != KMASSIGN_OK)
         return rc;
-    float *norms = reinterpret_cast<float *>(scratch);
-    unsigned long long *keys = nullptr;
-    if (cnorm == nullptr) {
-        // Every norm the kernel reads is written here first.
-        if (kma::launch_norms(C, K, D, norms, stream) != cudaSuccess)
-            return KMASSIGN_ERR_CUDA;
-        cnorm = norms;
-    }
+    // The array keeps the previous call's contents: the preparation launch
+    // writes every norm the kernel reads and resets the split rows' keys and
+    // counters.
+    float *norms = cnorm == nullptr ? reinterpret_cast<float *>(scratch) : nullptr;
     const int64_t row_split = split_first_row(plan);
     const int64_t n_split = plan.ksplit > 1 ? N - row_split : 0;
-    if (n_split > 0) {
-        // The array keeps the previous call's keys: reset them to "no candidate".
-        keys = reinterpret_cast<unsigned long long *>(scratch + kNoAllocNormBytes);
-        if (cudaMemsetAsync(keys, 0xff, static_cast<size_t>(n_split) * 8, stream) != cudaSuccess)
-            return KMASSIGN_ERR_CUDA;
-    }
-    const AssignParams p = make_params(plan, cnorm, idx, minscore, keys, N, K, D);
+    unsigned char *split = n_split > 0 ? scratch + kNoAllocNormBytes : nullptr;
+    const size_t split_bytes = n_split > 0 ? kma::split_scratch_bytes(n_split) : 0;
+    if ((norms != nullptr || split != nullptr) &&
+        kma::launch_prep(C, K, D, cnorm, norms, nullptr, split, split_bytes, stream) !=
+            cudaSuccess)
+        return KMASSIGN_ERR_CUDA;
+    AssignParams p = make_params(plan, cnorm != nullptr ? cnorm : norms, idx, minscore,
+                                 reinterpret_cast<unsigned long long *>(split), N, K, D);
+    if (split != nullptr)
+        p.counters = reinterpret_cast<uint32_t *>(split + kma::split_counter_offset(n_split));
     const CUtensorMap no_fold{};
     if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, no_fold, plan.grid, plan.smem,
                            stream) != cudaSuccess)
-        return KMASSIGN_ERR_CUDA;
-    if (keys != nullptr &&
-        kma::launch_finalize(keys, n_split, idx + row_split,
-                             minscore ? minscore + row_split : nullptr, stream) != cudaSuccess)
         return KMASSIGN_ERR_CUDA;
     return KMASSIGN_OK;
 }

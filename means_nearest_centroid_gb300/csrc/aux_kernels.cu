@@ -1,20 +1,21 @@
-// aux_kernels.cu -- the centroid-norm kernel, the key-finalize kernel, the
-// new-centroid kernel of the update step and the distance fix-up.
+// aux_kernels.cu -- the centroid-norm kernel, the preparation kernel of an
+// assignment call, the new-centroid kernel of the update step and the
+// distance fix-up.
 //
 // Norms (flashlib PR #22 "Optimize Blackwell k-means assignment reduction",
 // Summary: the centroid norms applied to every score tile):
-//   cnorm[j] = sum_d c_jd^2, fp32, one warp per centroid row.  Each lane
+//   cnorm[j] = sum_d c_jd^2, fp32, one warp per centroid row (warp_row_norm:
+//   a fixed summation order, so the result is deterministic).  Each lane
 //   reads 16 contiguous bytes (8 bf16) of the row, so a warp reads a 512-byte
-//   row in one coalesced sweep; D <= 256 means one load per lane.  Each lane
-//   sums its 8 exact squares in order, then a fixed xor-shuffle tree adds the
-//   lanes, so the result is deterministic.  The kernel is bound by HBM
-//   bandwidth (2*D bytes read, 4 written per centroid).
+//   row in one coalesced sweep.  Bound by HBM bandwidth (2*D bytes read, 4
+//   written per centroid).
 //
-// Finalize: turns the packed (ordered score << 32 | index) keys left by the
-// split-centroid path into idx and minscore.  A key still at its initial
-// all-ones value means no number was seen for that point (every score NaN):
-// idx 0, minscore NaN.
+// Preparation: everything an assignment call needs before its main kernel,
+// in one launch -- the norms (when the caller gave none), the CTA pair's fold
+// operand (when the plan folds the norms on CTA pairs), and the all-ones
+// initial value of the packed keys and arrival counters of split rows.
 #include "internal.h"
+#include "norm_math.cuh"
 
 #include <cuda_bf16.h>
 
@@ -32,47 +33,61 @@ __global__ void __launch_bounds__(32 * kNormWarps)
     const int64_t j = static_cast<int64_t>(blockIdx.x) * kNormWarps + (threadIdx.x >> 5);
     if (j >= K)
         return;
-    const int vec_per_row = D >> 3;   // 16-byte vectors per row (D % 16 == 0)
-    float acc = 0.0f;
-    if (lane < vec_per_row) {
-        const uint4 q = __ldg(C + j * vec_per_row + lane);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float lo = __uint_as_float(w[i] << 16);
-            const float hi = __uint_as_float(w[i] & 0xffff0000u);
-            acc = fmaf(lo, lo, acc);
-            acc = fmaf(hi, hi, acc);
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const float acc = warp_row_norm(C + j * (D >> 3), D, lane);
     if (lane == 0)
         cnorm[j] = acc;
 }
 
-__global__ void finalize_kernel(const unsigned long long *__restrict__ keys, int64_t N,
-                                int32_t *__restrict__ idx, float *__restrict__ minscore)
+struct PrepArgs {
+    const uint4 *C;          // centroids, or nullptr when the norms are given
+    const float *cnorm_in;   // the caller's norms, or nullptr
+    float *cnorm_out;        // norms computed here, or nullptr
+    uint4 *fold;             // fold operand ([block][2][128] rows of 16 bytes), or nullptr
+    uint4 *fill;             // 16-byte words set to all-ones, or nullptr
+    int64_t K, rows, fill_words;
+    int64_t row_blocks;      // blocks [0, row_blocks) work on centroid rows
+    int32_t D;
+};
+
+// Rows: one warp per centroid row j < rows (rows covers K, and the fold
+// operand's padding to whole blocks of 128 centroids per CTA, whose rows
+// hold NaN so that they never win).  The fold operand of centroid j is row r
+// = j % 128 of block b = j / 128: its first K half holds the three bf16 parts
+// of -cnorm[j] / 2, its second half zeros.  Fill: the remaining blocks write
+// all-ones words.
+__global__ void __launch_bounds__(32 * kNormWarps) prep_kernel(const PrepArgs a)
 {
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= N)
+    if (blockIdx.x >= a.row_blocks) {
+        const int64_t stride = (static_cast<int64_t>(gridDim.x) - a.row_blocks) * blockDim.x;
+        for (int64_t t = (static_cast<int64_t>(blockIdx.x) - a.row_blocks) * blockDim.x +
+                         threadIdx.x;
+             t < a.fill_words; t += stride)
+            a.fill[t] = make_uint4(~0u, ~0u, ~0u, ~0u);
         return;
-    const unsigned long long key = keys[i];
-    int32_t ix;
-    float ms;
-    if (key == ~0ull) {
-        ix = 0;
-        ms = __int_as_float(0x7fc00000);
-    } else {
-        ix = static_cast<int32_t>(key & 0xffffffffull);
-        const uint32_t o = static_cast<uint32_t>(key >> 32);
-        const uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
-        ms = __uint_as_float(u);
     }
-    idx[i] = ix;
-    if (minscore != nullptr)
-        minscore[i] = ms;
+    const int lane = threadIdx.x & 31;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kNormWarps + (threadIdx.x >> 5);
+    if (j >= a.rows)
+        return;
+    float norm = __int_as_float(0x7fc00000);
+    if (j < a.K) {
+        if (a.cnorm_in != nullptr)
+            norm = __ldg(a.cnorm_in + j);
+        else
+            norm = warp_row_norm(a.C + j * (a.D >> 3), a.D, lane);
+    }
+    if (lane != 0)
+        return;
+    if (a.cnorm_out != nullptr && j < a.K)
+        a.cnorm_out[j] = norm;
+    if (a.fold != nullptr) {
+        uint32_t w0, w1;
+        fold_split(norm, w0, w1);
+        const int64_t b = j >> 7;
+        const int64_t r = j & 127;
+        a.fold[b * 256 + r] = make_uint4(w0, w1, 0u, 0u);
+        a.fold[b * 256 + 128 + r] = make_uint4(0u, 0u, 0u, 0u);
+    }
 }
 
 // New centroids from the sums: mean (fp32, correctly rounded division) where
@@ -169,12 +184,28 @@ cudaError_t launch_norms(const void *C, int64_t K, int64_t D, float *cnorm, cuda
     return cudaGetLastError();
 }
 
-cudaError_t launch_finalize(const unsigned long long *keys, int64_t N, int32_t *idx,
-                            float *minscore, cudaStream_t stream)
+cudaError_t launch_prep(const void *C, int64_t K, int64_t D, const float *cnorm_in,
+                        float *cnorm_out, void *fold, void *fill, size_t fill_bytes,
+                        cudaStream_t stream)
 {
-    const int threads = 256;
-    const int64_t blocks = (N + threads - 1) / threads;
-    finalize_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(keys, N, idx, minscore);
+    PrepArgs a{};
+    a.C = static_cast<const uint4 *>(C);
+    a.cnorm_in = cnorm_in;
+    a.cnorm_out = cnorm_out;
+    a.fold = static_cast<uint4 *>(fold);
+    a.fill = static_cast<uint4 *>(fill);
+    a.K = K;
+    a.D = static_cast<int32_t>(D);
+    a.rows = std::max<int64_t>(cnorm_out != nullptr ? K : 0,
+                               fold != nullptr ? fold_operand_blocks(K) * 128 : 0);
+    a.fill_words = fill != nullptr ? static_cast<int64_t>(fill_bytes / 16) : 0;
+    a.row_blocks = (a.rows + kNormWarps - 1) / kNormWarps;
+    const int64_t fill_blocks =
+        std::min<int64_t>((a.fill_words + 32 * kNormWarps - 1) / (32 * kNormWarps), 1024);
+    const int64_t blocks = a.row_blocks + fill_blocks;
+    if (blocks == 0)
+        return cudaSuccess;
+    prep_kernel<<<static_cast<unsigned>(blocks), 32 * kNormWarps, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,10 @@ struct AssignParams {
     // row - split_row0 * rows per tile: one per row for the assignment, L per
     // (row, centroid range) for the k-nearest kernel.
     unsigned long long *keys;
+    // Arrival counters of the split rows, one per group of 128 (all-ones
+    // before the launch): the last of a group's ksplit units turns its keys
+    // into idx and minscore.
+    uint32_t *counters;
     int32_t topk;                  // k of the k-nearest kernel (idx, minscore hold [N, k])
     const float *xnorm;            // [N] ||x||^2: the k-nearest kernel writes distances
     int32_t N, K, D;
@@ -68,13 +72,12 @@ cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
 bool assign_folds(const Variant &v, int kblocks);
 // The CTA pair's fold operand: fold_operand_blocks(K) blocks of 128
 // centroids, 4 KiB each ([K half][128 rows][16 B] bf16), written from the
-// norms by launch_fold_operand (rows past K hold NaN).
+// norms by launch_prep (rows past K hold NaN).
 int64_t fold_operand_blocks(int64_t K);
 // Fold-operand slots of a folding CTA pair with `stages` C stages: one per
 // tile the C ring holds (at least 2, at most kMaxStages).
 int pair_fold_stages(int kblocks, int stages);
 size_t fold_operand_bytes(int64_t K);
-cudaError_t launch_fold_operand(const float *cnorm, int64_t K, void *out, cudaStream_t stream);
 
 // The k-nearest kernel: one shape (256 points x 128 centroids per tile, 8
 // consumer warps), a sorted list of `list` in {4, 8, 16, 32} >= k candidates
@@ -106,8 +109,16 @@ cudaError_t launch_centroids(const float *sums, const int32_t *counts, const voi
                              int64_t D, void *C_new, float *means, cudaStream_t stream);
 // score[i] = max(xnorm[i] + score[i], 0) (NaN kept): distances from scores.
 cudaError_t launch_add_norms(float *score, const float *xnorm, int64_t N, cudaStream_t stream);
-cudaError_t launch_finalize(const unsigned long long *keys, int64_t N, int32_t *idx,
-                            float *minscore, cudaStream_t stream);
+// One launch before an assignment kernel, doing any of: the norms of C into
+// cnorm_out (when cnorm_in is NULL), the fold operand from the norms (when
+// fold is not NULL), and fill_bytes (a multiple of 16) of all-ones at fill.
+cudaError_t launch_prep(const void *C, int64_t K, int64_t D, const float *cnorm_in,
+                        float *cnorm_out, void *fold, void *fill, size_t fill_bytes,
+                        cudaStream_t stream);
+// Bytes of packed keys and arrival counters for n_split split rows (a
+// multiple of 16; the counters start at byte split_counter_offset).
+size_t split_scratch_bytes(int64_t n_split);
+size_t split_counter_offset(int64_t n_split);
 
 // Read and clear the device status word of the assignment kernels, and of
 // the k-nearest kernels (0 or a kmassign_status code).

@@ -15,6 +15,7 @@
 #pragma once
 
 #include "internal.h"
+#include "norm_math.cuh"
 #include "ptx.cuh"
 
 #include "kmassign.h"
@@ -41,7 +42,7 @@ constexpr int kBarCnEmpty = kBarCnFull + kCnStages;   // [kCnStages]
 constexpr int kBarFoldFull = kBarCnEmpty + kCnStages; // [kMaxStages] CTA pair's fold ring
 constexpr int kBarFoldEmpty = kBarFoldFull + kMaxStages;   // [kMaxStages]
 constexpr int kNumBars = kBarFoldEmpty + kMaxStages;
-constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot + abort flag
+constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot, abort flag, 2 split flags
 // Norm folding (every assignment kernel at D <= 128, the k-nearest kernel at
 // every D): the norms enter the accumulator through one more K = 16 MMA step
 // per tile, A = a constant tile of ones, B = the tile's -||c||^2 / 2 split
@@ -62,6 +63,7 @@ constexpr uint32_t kFoldBlockBytes = 4096;
 constexpr uint32_t kFoldPairLbo = 2048;               // between the two K halves
 constexpr uint32_t kFoldPairSbo = 128;                // between 8-row groups
 constexpr uint32_t kConsumerBarrier = 1;              // named barrier id
+constexpr uint32_t kSplitBarrier = 2;                 // + sub-tile: a split row group's barrier
 // Bound on the teardown waits after an abort (copies and MMAs in flight
 // always finish; this only guards against a hardware failure).
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
@@ -445,31 +447,6 @@ __device__ __forceinline__ void fold_init(uint32_t fold_base)
         st_shared_v4_u32(fold_base + off, w, w, w, w);
     }
     fence_proxy_async_smem();
-}
-
-__device__ __forceinline__ uint32_t bf16_bits(float v)
-{
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
-}
-
-// -c / 2 (c a centroid norm, NaN past K) split into three bf16 parts
-// h + m + l, each the rounding of what the previous parts leave, so that
-// the sum carries the fp32 value's 24 bits; w0 = h | m << 16, w1 = l: the
-// first three K positions of the centroid's fold-operand row.  A non-finite
-// value goes whole into h.
-__device__ __forceinline__ void fold_split(float c, uint32_t &w0, uint32_t &w1)
-{
-    const float v = -0.5f * c;
-    if (isfinite(v)) {
-        const float h = __bfloat162float(__float2bfloat16_rn(v));
-        const float r = v - h;
-        const float m = __bfloat162float(__float2bfloat16_rn(r));
-        w0 = bf16_bits(h) | (bf16_bits(m) << 16);
-        w1 = bf16_bits(r - m);
-    } else {
-        w0 = bf16_bits(v);
-        w1 = 0u;
-    }
 }
 
 // Norm warp with FOLD: per tile, -||c_j||^2 / 2 for its NT centroids (NaN

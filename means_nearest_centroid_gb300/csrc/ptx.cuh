@@ -239,6 +239,35 @@ __device__ __forceinline__ void tmem_ld_red_max_32x32b_x32(uint32_t taddr, float
         v[i] = __uint_as_float(r[i]);
 }
 
+// Store of one float4 to shared memory by the lanes whose p is set (no branch).
+__device__ __forceinline__ void st_shared_v4_if(bool p, uint32_t addr, float a, float b, float c,
+                                                float d)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q st.shared.v4.f32 [%1], {%2, %3, %4, %5};\n\t}" ::"r"(static_cast<int>(p)),
+                 "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// The reducing load over 16 columns: 32 lanes x 16 values and each lane's
+// maximum of its 16 (same semantics as the 32-column form above).
+__device__ __forceinline__ void tmem_ld_red_max_32x32b_x16(uint32_t taddr, float *v, float &mx)
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=f"(mx)
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+
 // ---------------------------------------------------- CTA pairs (clusters of 2)
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
