@@ -715,29 +715,32 @@ def main():
         parity_info = {"rows": int(rows.size), "idx_differs": int(diff.size),
                        "outside_tolerance": bad}
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the C ABI with host buffers (kmassign_host)
     e2e = None
     if args.e2e_steps > 0:
         X0, C0 = sets[0]
         Xh = X0.pin_memory()
         Ch = C0.pin_memory()
+        cnh = None if norms_in_step else cns[0].cpu().pin_memory()
         idx_h = torch.empty(N, dtype=torch.int32).pin_memory()
-        scratch = {"C": dsets[1][1], "idx": idxs[1]}
-        km.assign_host(Xh, Ch, idx_h, device=device, scratch=scratch)
+        km.assign_host(Xh, Ch, idx_h, cnorm_host=cnh, device=device)
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            km.assign_host(Xh, Ch, idx_h, device=device, scratch=scratch)
+            km.assign_host(Xh, Ch, idx_h, cnorm_host=cnh, device=device)
         e2e_s = max_over_ranks(time.perf_counter() - t0, dist, device)
+        h2d = Xh.numel() * 2 + Ch.numel() * 2 + (0 if cnh is None else cnh.numel() * 4)
         e2e = {"value": flops * ws * args.e2e_steps / e2e_s / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": Xh.numel() * 2 + Ch.numel() * 2,
+               "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": idx_h.numel() * 4, "steps": args.e2e_steps,
                "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
-               "note": "every step: pinned host X and C copied in (X in row slices of whole waves overlapped "
-                       "with the assignment of the previous slice), norms + assignment, idx "
-                       "copied out, streams synchronised"}
+               "note": "every step one kmassign_host call (C ABI, pinned host buffers): C"
+                       + ("" if cnh is None else " and its norms") + " copied in, X in row "
+                       "slices of whole waves overlapped with the assignment of the previous "
+                       "slice, " + ("norms + " if cnh is None else "") + "assignment, idx "
+                       "copied out per slice; the call returns when idx is in host memory"}
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
     cpu = None

@@ -33,7 +33,8 @@
  * Layout: every matrix is row-major and contiguous, D innermost.  Row pitch
  * is D * 2 bytes.  All pointers are device pointers (cudaMalloc, the stream
  * allocator or PyTorch CUDA tensors); host or unregistered pointers are
- * rejected with KMASSIGN_ERR_NOT_DEVICE before anything is launched.
+ * rejected with KMASSIGN_ERR_NOT_DEVICE before anything is launched.  The
+ * exception is kmassign_host (and _ex), which takes host buffers.
  *
  * Devices: the pointers' device is made current for the launches; the calling
  * thread's current device is restored before every entry point returns.
@@ -46,7 +47,9 @@
  * reserved between calls so that repeated calls do not re-map memory.
  *
  * Execution: every call is asynchronous on `stream` (a cudaStream_t passed as
- * void*; NULL is the legacy default stream) and never synchronises the host.
+ * void*; NULL is the legacy default stream) and never synchronises the host,
+ * except kmassign_check and the host-buffer call kmassign_host, which return
+ * once their stream's work is done.
  * Argument errors are returned before any launch; launch errors are returned
  * as KMASSIGN_ERR_CUDA.  The pipeline waits inside the main kernel are
  * bounded in time: a wait that runs out records KMASSIGN_ERR_TIMEOUT in a
@@ -73,7 +76,8 @@ enum kmassign_status {
     KMASSIGN_ERR_TIMEOUT = -6,       /* a bounded wait inside a kernel ran out */
     KMASSIGN_ERR_NOT_DEVICE = -7,    /* a pointer is not device memory */
     KMASSIGN_ERR_ARG = -8,           /* an invalid plan value, k or flag */
-    KMASSIGN_ERR_SCRATCH = -9        /* too large for kmassign_noalloc's static scratch */
+    KMASSIGN_ERR_SCRATCH = -9,       /* too large for kmassign_noalloc's static scratch */
+    KMASSIGN_ERR_NOT_HOST = -10      /* kmassign_host: a pointer is device memory */
 };
 
 /*
@@ -128,6 +132,52 @@ int kmassign(const void *X, const void *C, const float *cnorm, int64_t N, int64_
 int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
                 int64_t D, int32_t *idx, float *minscore, int ksplit, int rows_per_cta,
                 int centroids_per_tile, int consumer_warps, void *stream);
+
+/*
+ * kmassign for points, centroids and results held in HOST memory: the whole
+ * assignment step end to end, host to host (the Summary's operation, with
+ * the copies to and from the GPU inside the call).
+ *   X         host, bf16 [N, D] row-major
+ *   C         host, bf16 [K, D] row-major
+ *   cnorm     host fp32 [K], or NULL (then computed on the GPU)
+ *   N, K, D   as in kmassign (N == 0 does nothing and returns OK)
+ *   idx       host int32 [N], written
+ *   minscore  host fp32 [N] or NULL, written as in kmassign
+ *   stream    the caller's stream on the calling thread's current device
+ *             (NULL: the legacy default stream); the GPU work runs on it and
+ *             on two streams of the library, ordered after the work already
+ *             queued on it
+ * Host memory may be pinned (cudaHostAlloc, cudaHostRegister), pageable or
+ * managed; only pinned memory lets the copies overlap the kernels.  No
+ * alignment is required.  Device pointers return KMASSIGN_ERR_NOT_HOST.
+ *
+ * C (and cnorm) is copied first; X follows in row slices of about N / 8
+ * points, rounded to whole waves of the assignment kernel's thread blocks,
+ * through two device buffers: the copy of one slice overlaps the assignment
+ * of the previous one, and each slice's answers are copied back while the
+ * next slice runs.  Each slice is one kmassign call, so the results are
+ * kmassign's bits for the whole batch.  Device temporaries (C, the norms,
+ * two X slices, two idx and minscore slices) come from the library's
+ * stream-ordered pool and are returned before the call ends.
+ *
+ * Synchronous: returns once idx and minscore hold the answers and every
+ * temporary is released.  A pipeline wait that ran out in one of the
+ * kernels returns KMASSIGN_ERR_TIMEOUT and clears the device status word as
+ * kmassign_check does.  The first call on a device creates the library's two
+ * streams and events there (kept until the process exits).  Calls on one
+ * device are serialised.
+ */
+int kmassign_host(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                  int64_t D, int32_t *idx, float *minscore, void *stream);
+
+/*
+ * kmassign_host with the slice size forced: rows_per_slice > 0 points per
+ * slice (the last takes the rest), 0 the automatic choice above; negative
+ * returns KMASSIGN_ERR_ARG.  The results do not depend on it.
+ */
+int kmassign_host_ex(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K,
+                     int64_t D, int32_t *idx, float *minscore, int64_t rows_per_slice,
+                     void *stream);
 
 /*
  * The plan kmassign would choose for (N, K, D) on the current device:

@@ -40,6 +40,7 @@ STATUS = {
     "KMASSIGN_ERR_NOT_DEVICE": -7,
     "KMASSIGN_ERR_ARG": -8,
     "KMASSIGN_ERR_SCRATCH": -9,
+    "KMASSIGN_ERR_NOT_HOST": -10,
 }
 _NAMES = {v: k for k, v in STATUS.items()}
 
@@ -65,6 +66,10 @@ def _declare(lib):
     lib.kmassign.restype = i32
     lib.kmassign_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, i32, i32, i32, i32, vp]
     lib.kmassign_ex.restype = i32
+    lib.kmassign_host.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp]
+    lib.kmassign_host.restype = i32
+    lib.kmassign_host_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, i64, vp]
+    lib.kmassign_host_ex.restype = i32
     lib.kmassign_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.kmassign_noalloc.restype = i32
     lib.kmassign_plan.argtypes = [i64, i64, i64, vp]
@@ -378,110 +383,51 @@ def assign(X, C, cnorm=None, with_minscore: bool = False, stream=None):
     return (idx, ms) if with_minscore else idx
 
 
-def _slices(N: int, chunks: int, first_rows, align: int = 1):
-    """Row boundaries of the X slices: ``first_rows`` for the first (its copy
-    is the only one nothing overlaps; default an even share), then the rest in
-    equal parts.  With ``align`` > 1 (the rows one wave of the assignment's
-    work units covers) the even share is rounded to a whole number of waves,
-    so that no slice but the last ends in a partly filled wave; the last slice
-    takes what remains."""
-    chunks = max(1, min(int(chunks), max(1, N)))
-    if chunks == 1 or N == 0:
-        return [0, N]
-    align = max(1, int(align))
-    share = -(-N // chunks)
-    if align > 1:
-        share = max(align, int(round(share / align)) * align)
-    if first_rows is None:
-        first_rows = share
-    first = max(1, min(int(first_rows), N))
-    rest = N - first
-    if align > 1:
-        per = share
-    else:
-        per = -(-rest // (chunks - 1)) if rest else 0
-    bounds = [0, first]
-    while bounds[-1] < N:
-        bounds.append(min(N, bounds[-1] + per))
-    return bounds
+def _need_host(t, name, dtype):
+    if isinstance(t, torch.Tensor) and not t.is_cuda and t.dtype == dtype and t.is_contiguous():
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a CPU tensor (ideally pinned)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    raise ValueError(f"{name} must be contiguous")
 
 
-def _wave_rows(N: int, K: int, D: int) -> int:
-    """Rows one full wave of the assignment's work units covers for this
-    shape (blocks in flight times rows per block; a CTA pair counts once)."""
-    p = kmassign_plan(max(N, 1), K, D)
-    pair = p["rows_per_cta"] == 256 and p["centroids_per_tile"] == 256
-    units = p["grid"] // 2 if pair else p["grid"]
-    return max(1, units * p["rows_per_cta"])
+def assign_host(X_host, C_host, idx_host=None, cnorm_host=None, minscore_host=None,
+                device=None, stream=None, rows_per_slice: int = 0):
+    """End-to-end assignment of host tensors through ``kmassign_host``.
 
-
-def assign_host(X_host, C_host, idx_host=None, device=None, stream=None, scratch=None,
-                chunks: int = 8, first_rows=None):
-    """End-to-end assignment of host tensors (X and C ideally pinned).
-
-    C is copied and its norms computed first; X is copied in ``chunks`` row
-    slices through two device buffers on a copy stream while the previous
-    slice is assigned on the compute stream, and each slice's idx is copied
-    back on a third stream as soon as it is ready.  ``first_rows`` sets the
-    first slice's size (default: even slices; on GB300 a shorter first slice
-    measured no gain, since the kernel itself slows while copies run).  Every
-    step of the method still runs in the
-    library's kernels; this only overlaps the host<->device copies with them.
-    ``scratch`` may hold preallocated device tensors {"X", "C", "idx"} (X of
-    at least two slices' rows, C of C_host's shape, idx of N rows).  Returns
-    ``idx_host`` (pinned int32, allocated if None) after synchronising.
+    X (bf16 [N, D]), C (bf16 [K, D]) and the optional cnorm (fp32 [K]) are
+    CPU tensors, ideally pinned so that the copies overlap the kernels.  The
+    library copies C in, then X in row slices of whole kernel waves while the
+    previous slice is assigned, and copies each slice's idx (and minscore)
+    back as soon as it is ready; the call returns when the answers are in
+    ``idx_host`` (int32 [N], pinned, allocated if None) and ``minscore_host``
+    (fp32 [N] or None).  ``device`` is the GPU to run on (default: current),
+    ``stream`` a stream of it (default: its current stream),
+    ``rows_per_slice`` forces the slice size (0: automatic).  Returns idx_host.
     """
-    device = torch.device("cuda") if device is None else torch.device(device)
-    compute = torch.cuda.current_stream(device) if stream is None else stream
+    _need_host(X_host, "X_host", torch.bfloat16)
+    _need_host(C_host, "C_host", torch.bfloat16)
     N, D = X_host.shape
-    if scratch is None:
-        scratch = {}
+    K, D2 = C_host.shape
+    if D != D2:
+        raise ValueError("X and C disagree on D")
+    if cnorm_host is not None:
+        _need_host(cnorm_host, "cnorm_host", torch.float32)
     if idx_host is None:
         idx_host = torch.empty(N, dtype=torch.int32, pin_memory=True)
-    bounds = _slices(N, chunks, first_rows, _wave_rows(N, C_host.shape[0], D) if N else 1)
-    rows = max((b - a for a, b in zip(bounds, bounds[1:])), default=0)
-    copy = scratch.get("copy_stream")
-    if copy is None:
-        copy = torch.cuda.Stream(device)
-        scratch["copy_stream"] = copy
-    back = scratch.get("back_stream")          # idx copies must not delay X copies
-    if back is None:
-        back = torch.cuda.Stream(device)
-        scratch["back_stream"] = back
-    Cd = scratch.get("C")
-    if Cd is None or Cd.shape != C_host.shape:
-        Cd = torch.empty(C_host.shape, dtype=C_host.dtype, device=device)
-    Xbuf = scratch.get("X")
-    if Xbuf is None or Xbuf.shape[0] < 2 * rows or Xbuf.shape[1] != D:
-        Xbuf = torch.empty((2 * max(rows, 1), D), dtype=X_host.dtype, device=device)
-    idxd = scratch.get("idx")
-    if idxd is None or idxd.shape[0] < N:
-        idxd = torch.empty(max(N, 1), dtype=torch.int32, device=device)
-    cn = torch.empty(C_host.shape[0], dtype=torch.float32, device=device)
-    with torch.cuda.stream(compute):
-        Cd.copy_(C_host, non_blocking=True)
-        kmassign_norms(Cd, out=cn, stream=compute)
-    done = [None, None]          # compute finished with buffer slot b
-    for c, (b0, b1) in enumerate(zip(bounds, bounds[1:])):
-        if b0 >= b1:
-            break
-        slot = c % 2
-        xs = Xbuf[slot * rows:slot * rows + (b1 - b0)]
-        with torch.cuda.stream(copy):
-            if done[slot] is not None:
-                copy.wait_event(done[slot])
-            xs.copy_(X_host[b0:b1], non_blocking=True)
-            landed = torch.cuda.Event()
-            landed.record(copy)
-        compute.wait_event(landed)
-        kmassign(xs, Cd, cnorm=cn, idx=idxd[b0:b1], stream=compute)
-        fin = torch.cuda.Event()
-        fin.record(compute)
-        done[slot] = fin
-        with torch.cuda.stream(back):
-            back.wait_event(fin)
-            idx_host[b0:b1].copy_(idxd[b0:b1], non_blocking=True)
-    back.synchronize()
-    copy.synchronize()
-    compute.synchronize()
+    _need_host(idx_host, "idx_host", torch.int32)
+    if minscore_host is not None:
+        _need_host(minscore_host, "minscore_host", torch.float32)
+    device = torch.device("cuda") if device is None else torch.device(device)
+    if device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(device):
+        rc = library().kmassign_host_ex(_ptr(X_host), _ptr(C_host), _ptr(cnorm_host), N, K, D,
+                                        _ptr(idx_host), _ptr(minscore_host), int(rows_per_slice),
+                                        _stream_ptr(stream, device))
+    _check(rc, "kmassign_host")
     return idx_host

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkmassign.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["api.cu", "assign.cu", "topk.cu", "aux_kernels.cu", "update.cu"]
+SOURCES = ["api.cu", "assign.cu", "topk.cu", "aux_kernels.cu", "update.cu", "host_path.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "-I", INCLUDE]

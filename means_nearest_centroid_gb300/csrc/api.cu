@@ -540,6 +540,42 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
     return rc;
 }
 
+}  // namespace
+
+namespace kma {
+
+int library_pool(cudaMemPool_t *pool)
+{
+    DeviceInfo dev;
+    const int rc = current_device_info(&dev);
+    if (rc == KMASSIGN_OK)
+        *pool = dev.pool;
+    return rc;
+}
+
+int assign_wave_rows(int64_t N, int64_t K, int64_t D, int64_t *rows)
+{
+    int rc = check_shape(N, K, D);
+    if (rc != KMASSIGN_OK)
+        return rc;
+    DeviceInfo dev;
+    if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
+        return rc;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    Plan plan;
+    if ((rc = cached_plan(std::max<int64_t>(N, 1), K, D, dev, dev_id, 0, 0, 0, 0, &plan)) !=
+        KMASSIGN_OK)
+        return rc;
+    const int64_t blocks = plan.v.pair ? plan.grid / 2 : plan.grid;
+    *rows = std::max<int64_t>(1, blocks * (plan.v.pair ? 2 : plan.v.sub) * kma::kTileM);
+    return KMASSIGN_OK;
+}
+
+}  // namespace kma
+
+namespace {
+
 // The k nearest centroids of every point: idx and score hold [N, k] row-major;
 // distances selects ||x||^2 + s over s for score.
 int run_topk(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
@@ -1083,6 +1119,8 @@ const char *kmassign_strerror(int code)
         return "a bounded pipeline wait inside a kernel ran out; the kernel drained and returned";
     case KMASSIGN_ERR_NOT_DEVICE:
         return "a pointer is not device memory of the current device";
+    case KMASSIGN_ERR_NOT_HOST:
+        return "kmassign_host: a pointer is device memory, not host memory";
     case KMASSIGN_ERR_SCRATCH:
         return "kmassign_noalloc: K exceeds its static norm buffer (cnorm NULL needs K <= 1048576)";
     case KMASSIGN_ERR_ARG:

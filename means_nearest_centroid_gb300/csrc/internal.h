@@ -125,4 +125,11 @@ size_t split_counter_offset(int64_t n_split);
 cudaError_t status_read_and_clear(int *code);
 cudaError_t topk_status_read_and_clear(int *code);
 
+// For the host-buffer path (kmassign status codes): the stream-ordered memory
+// pool of the current device, and the points one full wave of the automatic
+// assignment plan covers (thread blocks in flight, a CTA pair counted once,
+// times points per block).
+int library_pool(cudaMemPool_t *pool);
+int assign_wave_rows(int64_t N, int64_t K, int64_t D, int64_t *rows);
+
 }  // namespace kma

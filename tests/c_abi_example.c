@@ -2,7 +2,8 @@
  * Calling libkmassign from plain C (no Python, no PyTorch): a tiny problem
  * with a known answer.  Centroid j is the one-hot vector e_j scaled by 2, and
  * point i equals centroid (i * 7) % K, so the nearest centroid of point i is
- * (i * 7) % K and its score ||c||^2 - 2 x.c = 4 - 8 = -4.
+ * (i * 7) % K and its score ||c||^2 - 2 x.c = 4 - 8 = -4.  The problem is
+ * solved from device buffers, then from host buffers (kmassign_host).
  * Exit status 0 when every check passes.
  */
 #include <stdint.h>
@@ -35,8 +36,8 @@ static uint16_t bf16(float f)
 int main(void)
 {
     static uint16_t hx[N * D], hc[K * D];
-    static int32_t hidx[N], htop[N * 2];
-    static float hms[N], hsc[N * 2];
+    static int32_t hidx[N], htop[N * 2], hidx2[N];
+    static float hms[N], hsc[N * 2], hms2[N];
     memset(hx, 0, sizeof hx);
     memset(hc, 0, sizeof hc);
     for (int j = 0; j < K; ++j)
@@ -80,6 +81,14 @@ int main(void)
         CHECK(htop[2 * i] == want && hsc[2 * i] == 0.0f, "top-1 distance");
         CHECK(htop[2 * i + 1] == (want == 0 ? 1 : 0) && hsc[2 * i + 1] == 8.0f, "top-2 distance");
     }
+    /* the same problem end to end from host buffers: copies inside the call */
+    CHECK(kmassign_host(hx, hc, NULL, N, K, D, hidx2, hms2, s) == KMASSIGN_OK, "kmassign_host");
+    for (int i = 0; i < N; ++i) {
+        CHECK(hidx2[i] == (i * 7) % K, "host idx");
+        CHECK(hms2[i] == -4.0f, "host minscore");
+    }
+    CHECK(kmassign_host(dx, dc, NULL, N, K, D, hidx2, NULL, s) == KMASSIGN_ERR_NOT_HOST,
+          "device pointers refused by kmassign_host");
     cudaStreamDestroy(s);
     cudaFree(dx);
     cudaFree(dc);

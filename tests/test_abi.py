@@ -154,3 +154,25 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mod.library(str(tmp_path / "missing.so"))
     finally:
         mod._lib = saved
+
+
+def host_call(lib, X=A16, C=A16B, cn=NULL, N=10, K=5, D=64, idx=A16, ms=NULL, rows=0):
+    return lib.kmassign_host_ex(X, C, cn, N, K, D, idx, ms, rows, NULL)
+
+
+def test_host_path_argument_errors(lib):
+    """kmassign_host checks its arguments before touching CUDA."""
+    S = km.STATUS
+    assert host_call(lib, N=-1) == S["KMASSIGN_ERR_SHAPE"]
+    assert host_call(lib, K=0) == S["KMASSIGN_ERR_SHAPE"]
+    for D in (0, 8, 24, 272):
+        assert host_call(lib, D=D) == S["KMASSIGN_ERR_UNSUPPORTED_D"], D
+    assert host_call(lib, rows=-1) == S["KMASSIGN_ERR_ARG"]
+    assert host_call(lib, X=NULL, idx=NULL, N=0) == 0
+    assert host_call(lib, X=NULL) == S["KMASSIGN_ERR_NULL"]
+    assert host_call(lib, C=NULL) == S["KMASSIGN_ERR_NULL"]
+    assert host_call(lib, idx=NULL) == S["KMASSIGN_ERR_NULL"]
+    # no alignment is required of host buffers: a misaligned pointer passes
+    # the checks and fails only for want of a GPU here
+    assert lib.kmassign_host(MIS, A16B, NULL, 10, 5, 64, A16, NULL, NULL) != \
+        S["KMASSIGN_ERR_ALIGN"]

@@ -240,33 +240,80 @@ def test_assign_host_end_to_end(dev):
     assert rep.ok(), rep
 
 
-@pytest.mark.parametrize("N,chunks", [(3, 4), (1001, 4), (5000, 3), (777, 1), (6000, 8)])
-def test_assign_host_chunked_matches_device_call(dev, N, chunks):
-    X, C = workloads.blobs(N, 300, 64, seed=N)
-    got = km.assign_host(X.pin_memory(), C.pin_memory(), chunks=chunks)
-    ref = km.kmassign(X.to(dev), C.to(dev)).cpu()
-    assert torch.equal(got, ref)
+def _host_call(X, C, cnorm=None, minscore=False, rows=0, pin=True):
+    """kmassign_host_ex straight through the C ABI with host buffers."""
+    N, D = X.shape
+    K = C.shape[0]
+    hold = (lambda t: t.pin_memory()) if pin else (lambda t: t.contiguous())
+    Xh, Ch = hold(X), hold(C)
+    cn = None if cnorm is None else hold(cnorm)
+    idx = hold(torch.full((N,), -1, dtype=torch.int32))
+    ms = hold(torch.full((N,), 7.0)) if minscore else None
+    rc = km.library().kmassign_host_ex(km._ptr(Xh), km._ptr(Ch), km._ptr(cn), N, K, D,
+                                       km._ptr(idx), km._ptr(ms), rows, km._stream_ptr(None))
+    return rc, idx, ms
 
 
-@pytest.mark.parametrize("D,K", [(96, 16384), (128, 4096), (128, 16384)])
-def test_assign_host_slices_match_whole_call_folding_pairs(dev, D, K):
-    """At D = 96 and 128, where the whole call runs on CTA pairs and the
-    slices of the host path on other shapes, the slices still give the whole
-    call's bits."""
-    N = 90000
-    X, C = workloads.iid(N, K, D, seed=D + K)
-    plan = km.kmassign_plan(N, K, D)
-    assert (plan["rows_per_cta"], plan["centroids_per_tile"]) == (256, 256), plan
-    got = km.assign_host(X.pin_memory(), C.pin_memory(), chunks=7)
-    ref = km.kmassign(X.to(dev), C.to(dev)).cpu()
-    assert torch.equal(got, ref)
+@pytest.mark.parametrize("N,K,D,gen", [
+    (70001, 3000, 64, workloads.integers),     # several slices, ragged last one
+    (5000, 16384, 96, workloads.integers),     # one slice, split centroid range
+    (40000, 700, 256, workloads.integers),
+])
+def test_host_path_matches_oracle_bit_exact(dev, N, K, D, gen):
+    """The host-buffer entry point against the oracle on integer data, where
+    every fp32 step is exact: idx and minscore bit for bit."""
+    X, C = gen(N, K, D, seed=N + K)
+    rc, idx, ms = _host_call(X, C, minscore=True)
+    assert rc == 0, km.kmassign_strerror(rc)
+    rep = parity.compare(X, C, idx, ms, integer=True)
+    assert rep.ok() and rep.idx_mismatches == 0, rep
 
 
-def test_assign_host_short_first_slice(dev):
-    X, C = workloads.blobs(4000, 300, 64, seed=40)
-    got = km.assign_host(X.pin_memory(), C.pin_memory(), chunks=5, first_rows=37)
-    ref = km.kmassign(X.to(dev), C.to(dev)).cpu()
-    assert torch.equal(got, ref)
+@pytest.mark.parametrize("N,K,D,rows", [
+    (3, 300, 64, 0), (1001, 300, 64, 250), (5000, 300, 64, 1), (6000, 1000, 128, 777),
+    (90000, 16384, 96, 0), (90000, 4096, 128, 20000), (50000, 2000, 192, 0),
+    (30000, 5000, 256, 4096),
+])
+def test_host_path_slices_match_whole_call(dev, N, K, D, rows):
+    """Any slicing (forced or automatic) gives the bits of one kmassign call
+    over all points, with the norms computed inside or given."""
+    X, C = workloads.blobs(N, K, D, seed=N + D)
+    Xd, Cd = X.to(dev), C.to(dev)
+    cn = km.kmassign_norms(Cd)
+    ref_ms = torch.empty(N, dtype=torch.float32, device=dev)
+    ref = km.kmassign(Xd, Cd, cnorm=cn, minscore=ref_ms).cpu()
+    for given in (False, True):
+        rc, idx, ms = _host_call(X, C, cnorm=cn.cpu() if given else None, minscore=True,
+                                 rows=rows)
+        assert rc == 0, km.kmassign_strerror(rc)
+        assert torch.equal(idx, ref)
+        assert torch.equal(ms.view(torch.int32), ref_ms.cpu().view(torch.int32))
+
+
+def test_host_path_pageable_memory(dev):
+    """Pageable (unpinned) host buffers work too; the copies just do not overlap."""
+    X, C = workloads.blobs(20000, 500, 128, seed=3)
+    rc, idx, _ = _host_call(X, C, rows=3000, pin=False)
+    assert rc == 0
+    assert torch.equal(idx, km.kmassign(X.to(dev), C.to(dev)).cpu())
+
+
+def test_host_path_rejects_device_pointers(dev):
+    X, C = workloads.blobs(100, 50, 64, seed=4)
+    idx = torch.empty(100, dtype=torch.int32, device=dev)
+    rc = km.library().kmassign_host(km._ptr(X), km._ptr(C), None, 100, 50, 64, km._ptr(idx),
+                                    None, km._stream_ptr(None))
+    assert rc == km.STATUS["KMASSIGN_ERR_NOT_HOST"]
+
+
+def test_host_path_on_a_side_stream(dev):
+    """The caller's stream orders the call after its earlier work."""
+    X, C = workloads.blobs(8000, 900, 64, seed=5)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(1000000)
+        got = km.assign_host(X.pin_memory(), C.pin_memory(), stream=s, rows_per_slice=1500)
+    assert torch.equal(got, km.kmassign(X.to(dev), C.to(dev)).cpu())
 
 
 def test_non_default_stream(dev):
