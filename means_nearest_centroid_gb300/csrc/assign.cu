@@ -425,12 +425,14 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
 // precomputed fold operand like a C k-block); above, a norm ring serves the
 // epilogue as in the single-CTA kernel.  The stores are per CTA and identical
 // to the single-CTA kernel's.  Folded, the reduction differs in three ways,
-// all measured faster (1-6%) and bit-identical:
+// all measured faster and bit-identical:
 //   * each 32-column chunk is read as two 16-column reducing loads, and a
-//     lane that improves keeps only the 16-value half holding the chunk's
+//     lane that improves keeps only the 16-value half holding the group's
 //     first maximum (4 shared-memory stores instead of 8);
-//   * the improvement tests of a group of chunks are one branch-free chain,
-//     and only a lane's last improving chunk of the group is kept;
+//   * a warp tests its whole column slice of the tile at once: the largest t
+//     of the slice against the running best, one vote, and only when some
+//     lane improves the search for the first half holding that maximum
+//     (the best after the slice is its maximum at its first position);
 //   * the column slices of a row publish their running best per tile in
 //     shared memory and skip chunks strictly below another slice's best (a
 //     stale value only skips less; equal values are still kept, and the
@@ -650,6 +652,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                 for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
                     const uint32_t as = acc_used & 1u;
                     const uint32_t aph = (acc_used >> 1) & 1u;
+                    const uint32_t fb = fold_used % static_cast<uint32_t>(p.fold_stages);
+                    const uint32_t fph = (fold_used / static_cast<uint32_t>(p.fold_stages)) & 1u;
+                    if (kFold) {
+                        // Folded tiles are short (5 or 9 MMA steps), so the
+                        // accumulator hand-off is on the critical path: wait
+                        // for the tile's operands first (the copies run tiles
+                        // ahead), then for the stage, and issue at once.
+                        uint32_t s2 = stage, ph2 = phase;
+#pragma unroll
+                        for (int kb = 0; kb < KB; ++kb) {
+                            if (ok)
+                                ok = wait_warp(bar(kBarCFull + s2), ph2, abort_flag, p.timeout_ns);
+                            if (++s2 == static_cast<uint32_t>(p.stages)) {
+                                s2 = 0;
+                                ph2 ^= 1u;
+                            }
+                        }
+                        if (ok)
+                            ok = wait_warp(bar(kBarFoldFull + fb), fph, abort_flag, p.timeout_ns);
+                        if (!ok)
+                            break;
+                    }
                     if (!(ok = wait_warp(bar(kBarAccEmpty + as), aph ^ 1u, abort_flag,
                                          p.timeout_ns)))
                         break;
@@ -657,8 +681,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                     const uint32_t d_tmem = tmem_base + as * kAccCols;
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb) {
-                        if (!(ok = wait_warp(bar(kBarCFull + stage), phase, abort_flag,
-                                             p.timeout_ns)))
+                        if (!kFold && !(ok = wait_warp(bar(kBarCFull + stage), phase, abort_flag,
+                                                       p.timeout_ns)))
                             break;
                         const uint64_t cdesc = sw128_kmajor_desc(c_base + stage * kCStageBytes);
                         if (elect_one()) {
@@ -678,12 +702,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                     if (!ok)
                         break;
                     if (kFold) {
-                        const uint32_t fb = fold_used % static_cast<uint32_t>(p.fold_stages);
-                        const uint32_t fph =
-                            (fold_used / static_cast<uint32_t>(p.fold_stages)) & 1u;
-                        if (!(ok = wait_warp(bar(kBarFoldFull + fb), fph, abort_flag,
-                                             p.timeout_ns)))
-                            break;
                         const uint64_t bdesc =
                             plain_kmajor_desc(cn_base + kOnesBytes + fb * kFoldBlockBytes,
                                               kFoldPairLbo, kFoldPairSbo);
@@ -812,40 +830,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                         }
                         const int jg = tile * NT + col0 + g * kGroup * 32;
                         if (kFold) {
-                            bool imp[kGroup];
-                            bool hi[kGroup];
+                            // One test for the whole group: its largest t
+                            // (NaN only when every value is NaN, which never
+                            // improves).  The best after the group is that
+                            // maximum at its first position, so only when some
+                            // lane improves does the warp look for the first
+                            // 16-column half holding it and snapshot that half.
+                            float M = max2(m[0], mh[0]);
 #pragma unroll
-                            for (int c = 0; c < kGroup; ++c) {
-                                const float lo = m[c];
-                                m[c] = max2(lo, mh[c]);
-                                hi[c] = !(lo == m[c]);   // the first maximum is in the second half
-                            }
-                            float b = best;
-                            bool none = bi == kNone;
+                            for (int c = 1; c < kGroup; ++c)
+                                M = max3(M, m[c], mh[c]);
+                            const bool imp = ((M > best) || (M == best && bi == kNone)) &&
+                                             !(M < other);
+                            if (__any_sync(0xffffffffu, imp)) {
+                                bool found = !imp;
 #pragma unroll
-                            for (int c = 0; c < kGroup; ++c) {
-                                imp[c] = ((m[c] > b) || (m[c] == b && none)) && !(m[c] < other);
-                                b = imp[c] ? m[c] : b;
-                                none = none && !imp[c];
-                            }
-                            best = b;
-                            bool later = false;
+                                for (int c = 0; c < kGroup; ++c) {
 #pragma unroll
-                            for (int c = kGroup - 1; c >= 0; --c) {
-                                const bool st = imp[c] && !later;
-                                later = later || imp[c];
-                                if (__any_sync(0xffffffffu, st)) {
-                                    float h16[16];
+                                    for (int hf = 0; hf < 2; ++hf) {
+                                        const bool st = !found && ((hf ? mh[c] : m[c]) == M);
+                                        found = found || st;
 #pragma unroll
-                                    for (int k = 0; k < 16; ++k)
-                                        h16[k] = hi[c] ? v[c][16 + k] : v[c][k];
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i)
-                                        st_shared_v4_if(st, slot + 512u * i, h16[4 * i],
-                                                        h16[4 * i + 1], h16[4 * i + 2],
-                                                        h16[4 * i + 3]);
+                                        for (int i = 0; i < 4; ++i)
+                                            st_shared_v4_if(st, slot + 512u * i,
+                                                            v[c][16 * hf + 4 * i],
+                                                            v[c][16 * hf + 4 * i + 1],
+                                                            v[c][16 * hf + 4 * i + 2],
+                                                            v[c][16 * hf + 4 * i + 3]);
+                                        bi = st ? jg + 32 * c + 16 * hf : bi;
+                                    }
                                 }
-                                bi = st ? jg + 32 * c + (hi[c] ? 16 : 0) : bi;
+                                best = imp ? M : best;
                             }
                         } else {
 #pragma unroll

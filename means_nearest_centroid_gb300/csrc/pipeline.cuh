@@ -316,6 +316,7 @@ __device__ __forceinline__ void mma_role(const AssignParams &p, uint32_t x_base,
     constexpr uint32_t kXBufBytes = SUB * KB * kXTileBytes;
     constexpr uint32_t kAccCols = SUB * NT;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, NT);
+    constexpr bool kPreWait = FOLD && KB <= 2;
     auto bar = [&](int i) -> uint32_t { return bar_base + 8u * static_cast<uint32_t>(i); };
     uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0, fold_used = 0;
     bool ok = true, issued = false;
@@ -338,13 +339,36 @@ __device__ __forceinline__ void mma_role(const AssignParams &p, uint32_t x_base,
         for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
             const uint32_t as = acc_used & 1u;
             const uint32_t aph = (acc_used >> 1) & 1u;
+            const uint32_t fb = fold_used % kFoldStages;
+            const uint32_t fph = (fold_used / kFoldStages) & 1u;
+            if (kPreWait) {
+                // Short folded tiles: the operands (copied tiles ahead) are
+                // waited for before the accumulator stage, so the MMAs issue
+                // as soon as the consumers hand the stage back.  Only at
+                // KB <= 2: the ring always holds that many stages.
+                uint32_t s2 = stage, ph2 = phase;
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (ok)
+                        ok = wait_warp(bar(kBarCFull + s2), ph2, abort_flag, p.timeout_ns);
+                    if (++s2 == static_cast<uint32_t>(p.stages)) {
+                        s2 = 0;
+                        ph2 ^= 1u;
+                    }
+                }
+                if (ok)
+                    ok = wait_warp(bar(kBarCnFull + fb), fph, abort_flag, p.timeout_ns);
+                if (!ok)
+                    break;
+            }
             if (!(ok = wait_warp(bar(kBarAccEmpty + as), aph ^ 1u, abort_flag, p.timeout_ns)))
                 break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + as * kAccCols;
 #pragma unroll
             for (int kb = 0; kb < KB; ++kb) {
-                if (!(ok = wait_warp(bar(kBarCFull + stage), phase, abort_flag, p.timeout_ns)))
+                if (!kPreWait &&
+                    !(ok = wait_warp(bar(kBarCFull + stage), phase, abort_flag, p.timeout_ns)))
                     break;
                 const uint64_t cdesc = sw128_kmajor_desc(c_base + stage * kCStageBytes);
                 if (elect_one()) {
@@ -368,9 +392,8 @@ __device__ __forceinline__ void mma_role(const AssignParams &p, uint32_t x_base,
             if (!ok)
                 break;
             if (FOLD) {
-                const uint32_t fb = fold_used % kFoldStages;
-                const uint32_t fph = (fold_used / kFoldStages) & 1u;
-                if (!(ok = wait_warp(bar(kBarCnFull + fb), fph, abort_flag, p.timeout_ns)))
+                if (!kPreWait &&
+                    !(ok = wait_warp(bar(kBarCnFull + fb), fph, abort_flag, p.timeout_ns)))
                     break;
                 const uint64_t bdesc =
                     plain_kmajor_desc(fold_base + kOnesBytes + fb * NT * 32u, kFoldLbo, kFoldSbo);
