@@ -518,9 +518,10 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
         (split_bytes > 0 && !take(reinterpret_cast<void **>(&split), split_bytes)))
         rc = KMASSIGN_ERR_CUDA;
     CUtensorMap fmap{};
+    bool prepped = false;
     if (rc == KMASSIGN_OK && (tmp_norm != nullptr || fold != nullptr || split != nullptr)) {
-        if (kma::launch_prep(C, K, D, cnorm, tmp_norm, fold, split, split_bytes, stream) !=
-                cudaSuccess ||
+        if (kma::launch_prep(C, K, D, cnorm, tmp_norm, fold, split, split_bytes, stream,
+                             &prepped) != cudaSuccess ||
             (fold != nullptr && !encode_fold_map(&fmap, fold, K)))
             rc = KMASSIGN_ERR_CUDA;
     }
@@ -531,7 +532,7 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
             p.counters =
                 reinterpret_cast<uint32_t *>(split + kma::split_counter_offset(n_split));
         if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, fmap, plan.grid, plan.smem,
-                               stream) != cudaSuccess)
+                               stream, prepped) != cudaSuccess)
             rc = KMASSIGN_ERR_CUDA;
     }
     for (void *t : {static_cast<void *>(split), fold, static_cast<void *>(tmp_norm)})
@@ -966,8 +967,9 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
     const int64_t n_split = plan.ksplit > 1 ? N - row_split : 0;
     unsigned char *split = n_split > 0 ? scratch + kNoAllocNormBytes : nullptr;
     const size_t split_bytes = n_split > 0 ? kma::split_scratch_bytes(n_split) : 0;
+    bool prepped = false;
     if ((norms != nullptr || split != nullptr) &&
-        kma::launch_prep(C, K, D, cnorm, norms, nullptr, split, split_bytes, stream) !=
+        kma::launch_prep(C, K, D, cnorm, norms, nullptr, split, split_bytes, stream, &prepped) !=
             cudaSuccess)
         return KMASSIGN_ERR_CUDA;
     AssignParams p = make_params(plan, cnorm != nullptr ? cnorm : norms, idx, minscore,
@@ -976,7 +978,7 @@ int run_assign_noalloc(const void *X, const void *C, const float *cnorm, int64_t
         p.counters = reinterpret_cast<uint32_t *>(split + kma::split_counter_offset(n_split));
     const CUtensorMap no_fold{};
     if (kma::launch_assign(plan.v, p.kblocks, p, xmap, cmap, no_fold, plan.grid, plan.smem,
-                           stream) != cudaSuccess)
+                           stream, prepped) != cudaSuccess)
         return KMASSIGN_ERR_CUDA;
     return KMASSIGN_OK;
 }

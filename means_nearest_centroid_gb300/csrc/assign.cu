@@ -270,12 +270,14 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     } else if (warp == kMmaWarp) {
         mma_role<SUB, NT, KB, kFold>(p, x_base, c_base, bar_base, tmem_base, abort_flag, cn_base);
     } else if (warp == kNormWarp) {
+        grid_dep_wait();   // the norms may come from the preparation launch
         if (kFold)
             fold_norm_role<SUB, NT>(p, cn_base, bar_base, abort_flag);
         else
             norm_role<SUB, NT>(p, reinterpret_cast<float *>(sbase + (cn_base - base)), bar_base,
                                abort_flag);
     } else {
+        grid_dep_wait();   // split rows' keys and counters come from the preparation launch
         // Consumer warp w reads TMEM lanes 32*(w%4) .. +31 of sub-tile
         // (w/4)%SUB, columns [col0, col0 + kCW) of every tile.
         const int q = warp & 3;
@@ -549,6 +551,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     const int nclusters = static_cast<int>(gridDim.x >> 1);
 
     if (warp == kProducerWarp) {
+        if (kFold)
+            grid_dep_wait();   // the fold operand comes from the preparation launch
         if (lane == 0) {
             tma_prefetch_desc(&cmap);
             if (kFold)
@@ -733,6 +737,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
         }
     } else if (warp == kNormWarp) {
         // Folded, the norms come in with the fold operand: nothing to stage.
+        if (!kFold)
+            grid_dep_wait();   // the norms may come from the preparation launch
         float *const cn_smem = reinterpret_cast<float *>(sbase + (cn_base - base));
         const float kNaN = __int_as_float(0x7fc00000);
         uint32_t n = 0;
@@ -754,6 +760,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
             }
         }
     } else {
+        grid_dep_wait();   // split rows' keys and counters come from the preparation launch
         // Consumer warp w: TMEM lanes 32*(w%4) .. +31 of this CTA's 128 rows,
         // columns [col0, col0 + kCW) of every 256-column tile.
         const int q = warp & 3;
@@ -949,32 +956,55 @@ cudaError_t prepare_pair(size_t smem)
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
 }
 
+// Launch configuration; after_prep makes the launch the programmatic
+// dependent of the preparation kernel just before it in the stream.
+struct LaunchCfg {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    LaunchCfg(int grid, int threads, size_t smem, cudaStream_t stream, bool after_prep)
+    {
+        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+        cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = after_prep ? 1 : 0;
+    }
+};
+
 template <int CH, int KB>
 cudaError_t launch_pair(const AssignParams &p, const CUtensorMap &xmap, const CUtensorMap &cmap,
-                        const CUtensorMap &fmap, int grid, size_t smem, cudaStream_t stream)
+                        const CUtensorMap &fmap, int grid, size_t smem, cudaStream_t stream,
+                        bool after_prep)
 {
-    assign_pair_kernel<CH, KB><<<grid, 32 * (4 * CH + 4), smem, stream>>>(xmap, cmap, fmap, p);
-    return cudaGetLastError();
+    LaunchCfg lc(grid, 32 * (4 * CH + 4), smem, stream, after_prep);
+    return cudaLaunchKernelEx(&lc.cfg, assign_pair_kernel<CH, KB>, xmap, cmap, fmap, p);
 }
 
 template <int CH>
 cudaError_t dispatch_pair_kb(bool prepare, int kb, const AssignParams *p, const CUtensorMap *xmap,
                              const CUtensorMap *cmap, const CUtensorMap *fmap, int grid,
-                             size_t smem, cudaStream_t stream)
+                             size_t smem, cudaStream_t stream, bool after_prep)
 {
     switch (kb) {
     case 1:
         return prepare ? prepare_pair<CH, 1>(smem)
-                       : launch_pair<CH, 1>(*p, *xmap, *cmap, *fmap, grid, smem, stream);
+                       : launch_pair<CH, 1>(*p, *xmap, *cmap, *fmap, grid, smem, stream,
+                                                after_prep);
     case 2:
         return prepare ? prepare_pair<CH, 2>(smem)
-                       : launch_pair<CH, 2>(*p, *xmap, *cmap, *fmap, grid, smem, stream);
+                       : launch_pair<CH, 2>(*p, *xmap, *cmap, *fmap, grid, smem, stream,
+                                                after_prep);
     case 3:
         return prepare ? prepare_pair<CH, 3>(smem)
-                       : launch_pair<CH, 3>(*p, *xmap, *cmap, *fmap, grid, smem, stream);
+                       : launch_pair<CH, 3>(*p, *xmap, *cmap, *fmap, grid, smem, stream,
+                                                after_prep);
     case 4:
         return prepare ? prepare_pair<CH, 4>(smem)
-                       : launch_pair<CH, 4>(*p, *xmap, *cmap, *fmap, grid, smem, stream);
+                       : launch_pair<CH, 4>(*p, *xmap, *cmap, *fmap, grid, smem, stream,
+                                                after_prep);
     default:
         return cudaErrorInvalidValue;
     }
@@ -989,29 +1019,34 @@ cudaError_t prepare_one(size_t smem)
 
 template <int SUB, int NT, int CH, int KB>
 cudaError_t launch_one(const AssignParams &p, const CUtensorMap &xmap, const CUtensorMap &cmap,
-                       int grid, size_t smem, cudaStream_t stream)
+                       int grid, size_t smem, cudaStream_t stream, bool after_prep)
 {
-    assign_kernel<SUB, NT, CH, KB><<<grid, 32 * (4 * SUB * CH + 4), smem, stream>>>(xmap, cmap, p);
-    return cudaGetLastError();
+    LaunchCfg lc(grid, 32 * (4 * SUB * CH + 4), smem, stream, after_prep);
+    return cudaLaunchKernelEx(&lc.cfg, assign_kernel<SUB, NT, CH, KB>, xmap, cmap, p);
 }
 
 template <int SUB, int NT, int CH>
 cudaError_t dispatch_kb(bool prepare, int kb, const AssignParams *p, const CUtensorMap *xmap,
-                        const CUtensorMap *cmap, int grid, size_t smem, cudaStream_t stream)
+                        const CUtensorMap *cmap, int grid, size_t smem, cudaStream_t stream,
+                        bool after_prep)
 {
     switch (kb) {
     case 1:
         return prepare ? prepare_one<SUB, NT, CH, 1>(smem)
-                       : launch_one<SUB, NT, CH, 1>(*p, *xmap, *cmap, grid, smem, stream);
+                       : launch_one<SUB, NT, CH, 1>(*p, *xmap, *cmap, grid, smem, stream,
+                                                       after_prep);
     case 2:
         return prepare ? prepare_one<SUB, NT, CH, 2>(smem)
-                       : launch_one<SUB, NT, CH, 2>(*p, *xmap, *cmap, grid, smem, stream);
+                       : launch_one<SUB, NT, CH, 2>(*p, *xmap, *cmap, grid, smem, stream,
+                                                       after_prep);
     case 3:
         return prepare ? prepare_one<SUB, NT, CH, 3>(smem)
-                       : launch_one<SUB, NT, CH, 3>(*p, *xmap, *cmap, grid, smem, stream);
+                       : launch_one<SUB, NT, CH, 3>(*p, *xmap, *cmap, grid, smem, stream,
+                                                       after_prep);
     case 4:
         return prepare ? prepare_one<SUB, NT, CH, 4>(smem)
-                       : launch_one<SUB, NT, CH, 4>(*p, *xmap, *cmap, grid, smem, stream);
+                       : launch_one<SUB, NT, CH, 4>(*p, *xmap, *cmap, grid, smem, stream,
+                                                       after_prep);
     default:
         return cudaErrorInvalidValue;
     }
@@ -1019,25 +1054,32 @@ cudaError_t dispatch_kb(bool prepare, int kb, const AssignParams *p, const CUten
 
 cudaError_t dispatch(bool prepare, const Variant &v, int kb, const AssignParams *p,
                      const CUtensorMap *xmap, const CUtensorMap *cmap, const CUtensorMap *fmap,
-                     int grid, size_t smem, cudaStream_t stream)
+                     int grid, size_t smem, cudaStream_t stream, bool after_prep)
 {
     if (v.pair) {
         if (v.ch == 2)
-            return dispatch_pair_kb<2>(prepare, kb, p, xmap, cmap, fmap, grid, smem, stream);
+            return dispatch_pair_kb<2>(prepare, kb, p, xmap, cmap, fmap, grid, smem, stream,
+                                       after_prep);
         if (v.ch == 4)
-            return dispatch_pair_kb<4>(prepare, kb, p, xmap, cmap, fmap, grid, smem, stream);
+            return dispatch_pair_kb<4>(prepare, kb, p, xmap, cmap, fmap, grid, smem, stream,
+                                       after_prep);
         return cudaErrorInvalidValue;
     }
     if (v.sub == 1 && v.nt == 128 && v.ch == 1)
-        return dispatch_kb<1, 128, 1>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+        return dispatch_kb<1, 128, 1>(prepare, kb, p, xmap, cmap, grid, smem, stream,
+                                          after_prep);
     if (v.sub == 1 && v.nt == 256 && v.ch == 2)
-        return dispatch_kb<1, 256, 2>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+        return dispatch_kb<1, 256, 2>(prepare, kb, p, xmap, cmap, grid, smem, stream,
+                                          after_prep);
     if (v.sub == 2 && v.nt == 128 && v.ch == 1)
-        return dispatch_kb<2, 128, 1>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+        return dispatch_kb<2, 128, 1>(prepare, kb, p, xmap, cmap, grid, smem, stream,
+                                          after_prep);
     if (v.sub == 2 && v.nt == 128 && v.ch == 2)
-        return dispatch_kb<2, 128, 2>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+        return dispatch_kb<2, 128, 2>(prepare, kb, p, xmap, cmap, grid, smem, stream,
+                                          after_prep);
     if (v.sub == 1 && v.nt == 256 && v.ch == 4)
-        return dispatch_kb<1, 256, 4>(prepare, kb, p, xmap, cmap, grid, smem, stream);
+        return dispatch_kb<1, 256, 4>(prepare, kb, p, xmap, cmap, grid, smem, stream,
+                                          after_prep);
     return cudaErrorInvalidValue;
 }
 
@@ -1071,14 +1113,15 @@ size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 
 cudaError_t assign_prepare(const Variant &v, int kblocks, size_t smem)
 {
-    return dispatch(true, v, kblocks, nullptr, nullptr, nullptr, nullptr, 0, smem, nullptr);
+    return dispatch(true, v, kblocks, nullptr, nullptr, nullptr, nullptr, 0, smem, nullptr, false);
 }
 
 cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
                           const CUtensorMap &xmap, const CUtensorMap &cmap,
-                          const CUtensorMap &fmap, int grid, size_t smem, cudaStream_t stream)
+                          const CUtensorMap &fmap, int grid, size_t smem, cudaStream_t stream,
+                          bool after_prep)
 {
-    return dispatch(false, v, kblocks, &p, &xmap, &cmap, &fmap, grid, smem, stream);
+    return dispatch(false, v, kblocks, &p, &xmap, &cmap, &fmap, grid, smem, stream, after_prep);
 }
 
 cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int *clusters)

@@ -57,6 +57,9 @@ struct PrepArgs {
 // all-ones words.
 __global__ void __launch_bounds__(32 * kNormWarps) prep_kernel(const PrepArgs a)
 {
+    // The assignment kernel that follows may start its set-up now; its warps
+    // that read these outputs wait for this kernel to complete.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (blockIdx.x >= a.row_blocks) {
         const int64_t stride = (static_cast<int64_t>(gridDim.x) - a.row_blocks) * blockDim.x;
         for (int64_t t = (static_cast<int64_t>(blockIdx.x) - a.row_blocks) * blockDim.x +
@@ -186,8 +189,9 @@ cudaError_t launch_norms(const void *C, int64_t K, int64_t D, float *cnorm, cuda
 
 cudaError_t launch_prep(const void *C, int64_t K, int64_t D, const float *cnorm_in,
                         float *cnorm_out, void *fold, void *fill, size_t fill_bytes,
-                        cudaStream_t stream)
+                        cudaStream_t stream, bool *launched)
 {
+    *launched = false;
     PrepArgs a{};
     a.C = static_cast<const uint4 *>(C);
     a.cnorm_in = cnorm_in;
@@ -206,6 +210,7 @@ cudaError_t launch_prep(const void *C, int64_t K, int64_t D, const float *cnorm_
     if (blocks == 0)
         return cudaSuccess;
     prep_kernel<<<static_cast<unsigned>(blocks), 32 * kNormWarps, 0, stream>>>(a);
+    *launched = true;
     return cudaGetLastError();
 }
 

@@ -63,10 +63,17 @@ cudaError_t assign_prepare(const Variant &v, int kblocks, size_t smem_bytes);
 cudaError_t assign_max_clusters(const Variant &v, int kblocks, size_t smem, int *clusters);
 // fmap: the fold operand's tensor map, read only by kernels that fold the
 // norms into the MMA through it (assign_folds on a CTA pair); others ignore it.
+// after_prep: the launch directly before this one in the stream is the
+// call's preparation kernel.  The assignment kernel is then launched as its
+// programmatic dependent: its set-up (barriers, tensor memory, the X copies)
+// overlaps the preparation, and only the warps that read the preparation's
+// outputs (norms, fold operand, split keys) wait for it.  Everything queued
+// before the preparation kernel has completed when that kernel starts, so
+// the inputs are ready either way.
 cudaError_t launch_assign(const Variant &v, int kblocks, const AssignParams &p,
                           const CUtensorMap &xmap, const CUtensorMap &cmap,
                           const CUtensorMap &fmap, int grid, size_t smem_bytes,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool after_prep = false);
 // Whether the shape's kernel folds the norms into the MMA (every shape at up
 // to two k-blocks, D <= 128).
 bool assign_folds(const Variant &v, int kblocks);
@@ -112,9 +119,11 @@ cudaError_t launch_add_norms(float *score, const float *xnorm, int64_t N, cudaSt
 // One launch before an assignment kernel, doing any of: the norms of C into
 // cnorm_out (when cnorm_in is NULL), the fold operand from the norms (when
 // fold is not NULL), and fill_bytes (a multiple of 16) of all-ones at fill.
+// *launched tells whether a kernel was launched (nothing to do: none).  The
+// kernel lets the next launch in the stream start early (see launch_assign).
 cudaError_t launch_prep(const void *C, int64_t K, int64_t D, const float *cnorm_in,
                         float *cnorm_out, void *fold, void *fill, size_t fill_bytes,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool *launched);
 // Bytes of packed keys and arrival counters for n_split split rows (a
 // multiple of 16; the counters start at byte split_counter_offset).
 size_t split_scratch_bytes(int64_t n_split);

@@ -155,6 +155,16 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
                  : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched as the dependent of the
+// one before it in the stream may start while that one still runs; a thread
+// that reads what the earlier kernel writes first waits here for it to
+// complete and its writes to be visible (a no-op for a kernel not launched
+// that way).
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before()
 {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
