@@ -257,6 +257,36 @@ class NvmlClockSampler:
             self.thread.join(timeout=5)
             self.lib.nvmlShutdown()
 
+    def by_clock(self, t0, intervals, flops, sms, bin_mhz=50.0):
+        """Steps grouped by the SM clock seen while they ran: ``intervals``
+        holds each step's (start, end) in seconds after the timed region began
+        on the GPU (``t0`` in host time; the queue was empty then, so the GPU
+        starts within microseconds).  Per bin of ``bin_mhz``: the steps, their
+        mean kernel time and the rate per SM clock, so that a clock-bound and
+        a clock-independent limit can be told apart within one run."""
+        if not self.samples:
+            return None
+        import bisect
+        ts = [s[0] for s in self.samples]
+        bins = {}
+        for a, b in intervals:
+            i, j = bisect.bisect_left(ts, t0 + a), bisect.bisect_right(ts, t0 + b)
+            mhz = [self.samples[k][1] for k in range(i, j)]
+            if not mhz:   # no sample inside this step: the nearest one
+                k = min(max(i, 0), len(ts) - 1)
+                mhz = [self.samples[k][1]]
+            m = statistics.mean(mhz)
+            bins.setdefault(round(m / bin_mhz) * bin_mhz, []).append((b - a, m))
+        out = []
+        for c in sorted(bins):
+            v = bins[c]
+            ms = statistics.mean(d for d, _ in v) * 1e3
+            mhz = statistics.mean(m for _, m in v)
+            out.append({"sm_mhz": round(mhz), "steps": len(v), "kernel_ms": round(ms, 4),
+                        "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                        "flop_per_clk_per_sm": round(flops / (ms * 1e-3) / (sms * mhz * 1e6))})
+        return out
+
     def summary(self, t0, t1):
         inside = [s for s in self.samples if t0 <= s[0] <= t1]
         if not inside:
@@ -763,6 +793,13 @@ def main():
         # clock-normalised rate of the dominant kernel: flop per SM clock
         roofline["flop_per_clk_per_sm"] = achieved * 1e12 / (sms * clocks["sm_mhz"] * 1e6)
         roofline["sms"] = sms
+    if nvml.ok:
+        # each step's kernel interval on the GPU, paired with the clock then
+        spans = [(t_start.elapsed_time(m) * 1e-3, t_start.elapsed_time(e) * 1e-3)
+                 for m, e in zip(mids, ends)]
+        binned = nvml.by_clock(wall0, spans, flops, sms)
+        if binned:
+            clocks["by_clock"] = binned
     # the preparation launch (norms when computed in the step, the fold
     # operand of a CTA pair folding the norms at D <= 128, the split rows'
     # keys) and the assignment kernel, which also finalizes split rows
