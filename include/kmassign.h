@@ -77,7 +77,8 @@ enum kmassign_status {
     KMASSIGN_ERR_NOT_DEVICE = -7,    /* a pointer is not device memory */
     KMASSIGN_ERR_ARG = -8,           /* an invalid plan value, k or flag */
     KMASSIGN_ERR_SCRATCH = -9,       /* too large for kmassign_noalloc's static scratch */
-    KMASSIGN_ERR_NOT_HOST = -10      /* kmassign_host: a pointer is device memory */
+    KMASSIGN_ERR_NOT_HOST = -10,     /* kmassign_host: a pointer is device memory */
+    KMASSIGN_ERR_DEBUG_CHECK = -11   /* a device-side check of a KMASSIGN_DEBUG build failed */
 };
 
 /*
@@ -196,6 +197,20 @@ int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9);
  */
 int kmassign_plan_ex(int64_t N, int64_t K, int64_t D, int ksplit, int rows_per_cta,
                      int centroids_per_tile, int consumer_warps, int32_t *out9);
+
+/*
+ * The plan kmassign_ex would run with the same forcing arguments on a
+ * described device instead of the current one: sms streaming multiprocessors,
+ * smem_per_block bytes of opt-in shared memory per thread block, and
+ * pair_clusters two-block clusters of the CTA-pair kernel that can be
+ * resident at once (0: no CTA pairs; capped at sms / 2).  Host only: makes no
+ * CUDA call, so it also runs where no GPU is present (GB300: 152 SMs,
+ * 232,448 bytes, 76 pairs).  Layout of out9 and errors as kmassign_plan_ex;
+ * sms < 1 or a negative size returns KMASSIGN_ERR_ARG.
+ */
+int kmassign_plan_for(int64_t N, int64_t K, int64_t D, int sms, int smem_per_block,
+                      int pair_clusters, int ksplit, int rows_per_cta, int centroids_per_tile,
+                      int consumer_warps, int32_t *out9);
 
 /*
  * Synchronise `stream`, then report and clear the device status word:

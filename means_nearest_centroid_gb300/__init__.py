@@ -25,7 +25,7 @@ __all__ = [
     "KmassignError", "library", "library_path", "kmassign", "kmassign_ex", "kmassign_norms",
     "kmassign_noalloc", "kmassign_set_wait_timeout", "shard_rows", "kmassign_update",
     "kmassign_centroids", "kmassign_lloyd",
-    "kmassign_plan", "kmassign_check", "kmassign_strerror", "assign", "norms", "assign_host",
+    "kmassign_plan", "kmassign_plan_for", "kmassign_check", "kmassign_strerror", "assign", "norms", "assign_host",
     "STATUS",
 ]
 
@@ -41,6 +41,7 @@ STATUS = {
     "KMASSIGN_ERR_ARG": -8,
     "KMASSIGN_ERR_SCRATCH": -9,
     "KMASSIGN_ERR_NOT_HOST": -10,
+    "KMASSIGN_ERR_DEBUG_CHECK": -11,
 }
 _NAMES = {v: k for k, v in STATUS.items()}
 
@@ -76,6 +77,8 @@ def _declare(lib):
     lib.kmassign_plan.restype = i32
     lib.kmassign_plan_ex.argtypes = [i64, i64, i64, i32, i32, i32, i32, vp]
     lib.kmassign_plan_ex.restype = i32
+    lib.kmassign_plan_for.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, i32, vp]
+    lib.kmassign_plan_for.restype = i32
     lib.kmassign_update.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
     lib.kmassign_update.restype = i32
     lib.kmassign_update_ex.argtypes = [vp, vp, i64, i64, i64, vp, vp, i32, vp]
@@ -283,6 +286,21 @@ def kmassign_plan(N: int, K: int, D: int, ksplit: int = 0, rows_per_cta: int = 0
                                       int(centroids_per_tile), int(consumer_warps),
                                       ctypes.cast(out, ctypes.c_void_p)),
            "kmassign_plan")
+    keys = ["ksplit", "rows_per_cta", "centroids_per_tile", "grid", "stages", "xbufs",
+            "whole_row_tiles", "split_row_tiles", "consumer_warps"]
+    return dict(zip(keys, list(out)))
+
+
+def kmassign_plan_for(N: int, K: int, D: int, sms: int = 152, smem_per_block: int = 232448,
+                      pair_clusters: int = 76, ksplit: int = 0, rows_per_cta: int = 0,
+                      centroids_per_tile: int = 0, consumer_warps: int = 0) -> dict:
+    """The plan for a described device (default: a GB300); needs no GPU."""
+    out = (ctypes.c_int32 * 9)()
+    _check(library().kmassign_plan_for(int(N), int(K), int(D), int(sms), int(smem_per_block),
+                                       int(pair_clusters), int(ksplit), int(rows_per_cta),
+                                       int(centroids_per_tile), int(consumer_warps),
+                                       ctypes.cast(out, ctypes.c_void_p)),
+           "kmassign_plan_for")
     keys = ["ksplit", "rows_per_cta", "centroids_per_tile", "grid", "stages", "xbufs",
             "whole_row_tiles", "split_row_tiles", "consumer_warps"]
     return dict(zip(keys, list(out)))

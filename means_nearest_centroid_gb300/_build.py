@@ -41,23 +41,33 @@ def _deps():
             + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+# The debug build: the same sources with KMASSIGN_DEBUG defined (device-side
+# consistency checks that record KMASSIGN_ERR_DEBUG_CHECK), in a library and
+# object folder of its own so that it never replaces the normal build.
+DEBUG_DIR = os.path.join(BUILD_DIR, "debug")
+DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libkmassign_debug.so")
+
+
+def up_to_date(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile (if stale) and return the path of libkmassign.so."""
-    if not force and not extra_flags and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile (if stale) and return the path of libkmassign.so (with
+    ``debug``: of libkmassign_debug.so, built with KMASSIGN_DEBUG)."""
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    obj_dir = DEBUG_DIR if debug else BUILD_DIR
+    if not force and not extra_flags and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags)
+    flags = NVCC_FLAGS + list(extra_flags) + (["-DKMASSIGN_DEBUG"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -72,13 +82,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         for _, log in results:
             if log.strip():
                 print(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

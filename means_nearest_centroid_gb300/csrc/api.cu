@@ -1048,8 +1048,14 @@ int kmassign_topk_ex(const void *X, const void *C, const float *cnorm, int64_t N
                     static_cast<cudaStream_t>(stream));
 }
 
-int kmassign_plan_ex(int64_t N, int64_t K, int64_t D, int ksplit, int rows_per_cta,
-                     int centroids_per_tile, int consumer_warps, int32_t *out9)
+}  // extern "C"
+
+namespace {
+
+// kmassign_plan_ex and kmassign_plan_for: the forcing arguments' checks, the
+// planner, and the plan in the 9-value layout.
+int plan_to_out9(int64_t N, int64_t K, int64_t D, const DeviceInfo *dev_or_null, int ksplit,
+                 int rows_per_cta, int centroids_per_tile, int consumer_warps, int32_t *out9)
 {
     if (out9 == nullptr)
         return KMASSIGN_ERR_NULL;
@@ -1062,7 +1068,9 @@ int kmassign_plan_ex(int64_t N, int64_t K, int64_t D, int ksplit, int rows_per_c
          consumer_warps != 16))
         return KMASSIGN_ERR_ARG;
     DeviceInfo dev;
-    if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
+    if (dev_or_null != nullptr)
+        dev = *dev_or_null;
+    else if ((rc = current_device_info(&dev)) != KMASSIGN_OK)
         return rc;
     Plan plan;
     if ((rc = make_plan(std::max<int64_t>(N, 1), K, D, dev, ksplit, rows_per_cta,
@@ -1078,6 +1086,32 @@ int kmassign_plan_ex(int64_t N, int64_t K, int64_t D, int ksplit, int rows_per_c
     out9[7] = plan.rowtiles - plan.split_row0;
     out9[8] = 4 * plan.v.sub * plan.v.ch;
     return KMASSIGN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kmassign_plan_ex(int64_t N, int64_t K, int64_t D, int ksplit, int rows_per_cta,
+                     int centroids_per_tile, int consumer_warps, int32_t *out9)
+{
+    return plan_to_out9(N, K, D, nullptr, ksplit, rows_per_cta, centroids_per_tile,
+                        consumer_warps, out9);
+}
+
+int kmassign_plan_for(int64_t N, int64_t K, int64_t D, int sms, int smem_per_block,
+                      int pair_clusters, int ksplit, int rows_per_cta, int centroids_per_tile,
+                      int consumer_warps, int32_t *out9)
+{
+    if (sms < 1 || smem_per_block < 0 || pair_clusters < 0)
+        return KMASSIGN_ERR_ARG;
+    DeviceInfo dev;
+    dev.ready = true;
+    dev.sms = sms;
+    dev.smem_optin = smem_per_block;
+    dev.pair_clusters = std::min(pair_clusters, sms / 2);
+    return plan_to_out9(N, K, D, &dev, ksplit, rows_per_cta, centroids_per_tile, consumer_warps,
+                        out9);
 }
 
 int kmassign_plan(int64_t N, int64_t K, int64_t D, int32_t *out9)
@@ -1121,6 +1155,8 @@ const char *kmassign_strerror(int code)
         return "a bounded pipeline wait inside a kernel ran out; the kernel drained and returned";
     case KMASSIGN_ERR_NOT_DEVICE:
         return "a pointer is not device memory of the current device";
+    case KMASSIGN_ERR_DEBUG_CHECK:
+        return "a device-side consistency check of the debug build (KMASSIGN_DEBUG) failed";
     case KMASSIGN_ERR_NOT_HOST:
         return "kmassign_host: a pointer is device memory, not host memory";
     case KMASSIGN_ERR_SCRATCH:

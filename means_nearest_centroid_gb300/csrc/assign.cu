@@ -105,6 +105,12 @@ __device__ __forceinline__ void merge_split_group(const AssignParams &p, int row
                                                   bool counts)
 {
     const int64_t rel = row - static_cast<int64_t>(p.split_row0) * rows_per_unit;
+    if (kDebugChecks) {
+        // the keys and counters cover exactly the split rows
+        const int64_t n_split = p.N - static_cast<int64_t>(p.split_row0) * rows_per_unit;
+        store = store && debug_ok(rel >= 0 && rel < n_split);
+        counts = counts && debug_ok(rel >= 0 && (rel >> 7) < (n_split + 127) / 128);
+    }
     if (store && bi != kNone)
         atomicMin(p.keys + rel, pack_key(best, bi));
     __threadfence();
@@ -246,6 +252,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
     // last-unit flags of the split row groups (one per 128-row sub-tile)
     volatile uint32_t *split_flag = reinterpret_cast<volatile uint32_t *>(misc_ptr + 8);
     auto bar = [&](int i) -> uint32_t { return bar_base + 8u * static_cast<uint32_t>(i); };
+    if (!debug_layout_ok(p, bar_base - raw + kMiscBytes))
+        return;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -505,6 +513,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     const bool leader = rank == 0;
     // The leader's copy of barrier i, as a cluster address.
     auto lead_bar = [&](int i) -> uint32_t { return map_to_rank(bar(i), 0); };
+    if (!debug_layout_ok(p, bar_base - raw + kMiscBytes))
+        return;   // both CTAs of the pair decide alike
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < kMaxXBufs; ++b) {

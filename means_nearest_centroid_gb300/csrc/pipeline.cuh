@@ -73,6 +73,51 @@ __device__ __forceinline__ void record_timeout()
     atomicCAS(&g_status_word, 0, static_cast<int>(KMASSIGN_ERR_TIMEOUT));
 }
 
+// Debug build (compiled with KMASSIGN_DEBUG): device-side consistency checks
+// of what the host planned against what the kernels index -- the shared
+// memory layout against the launch's dynamic size, ring and buffer counts,
+// decoded work units against N and K, split-key indices against the split
+// rows.  A failed check records KMASSIGN_ERR_DEBUG_CHECK in the status word
+// (the first failure wins) and the access it guards is skipped or clamped;
+// nothing traps.  In the normal build every check is the constant true.
+#ifdef KMASSIGN_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+__device__ __forceinline__ bool debug_ok(bool cond)
+{
+    if (kDebugChecks && !cond)
+        atomicCAS(&g_status_word, 0, static_cast<int>(KMASSIGN_ERR_DEBUG_CHECK));
+    return !kDebugChecks || cond;
+}
+
+__device__ __forceinline__ uint32_t dynamic_smem_bytes()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+
+// The block's shared-memory layout ends at layout_end (bytes from the start
+// of dynamic shared memory, alignment padding included) and its rings are
+// within the compiled bounds.  Uniform across the block (and across a CTA
+// pair, which computes the same): a block that fails returns before it sets
+// anything up.
+__device__ __forceinline__ bool debug_layout_ok(const AssignParams &p, uint32_t layout_end)
+{
+    if (!kDebugChecks)
+        return true;
+    const bool ok = layout_end <= dynamic_smem_bytes() && p.stages >= 2 &&
+                    p.stages <= kMaxStages && p.xbufs >= 1 && p.xbufs <= kMaxXBufs &&
+                    p.fold_stages >= 2 && p.fold_stages <= kMaxStages && p.ksplit >= 1 &&
+                    p.chunk_tiles >= 1 && p.ntiles >= 1;
+    if (!ok && threadIdx.x == 0)
+        debug_ok(false);
+    return ok;
+}
+
 // Slow path of a bounded wait (the phase was not complete on first try).
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                        uint64_t limit_ns, bool honour_abort)
@@ -160,6 +205,13 @@ __device__ __forceinline__ Unit decode_unit(const AssignParams &p, int u)
     w.row0 = rt * SUB * kTileM;
     const int left = p.N - w.row0;
     w.nsub = min(SUB, (left + kTileM - 1) / kTileM);
+    if (kDebugChecks &&
+        !debug_ok(rt >= 0 && rt < p.rowtiles && left > 0 && w.t_begin >= 0 &&
+                  w.t_begin < w.t_end && w.t_end <= p.ntiles)) {
+        // clamped: an empty centroid range, every role alike
+        w.t_end = w.t_begin = 0;
+        w.nsub = max(w.nsub, 0);
+    }
     return w;
 }
 

@@ -74,3 +74,16 @@ def test_plan_ex_rejects_bad_forcing(dev):
                dict(consumer_warps=12)]:
         with pytest.raises(km.KmassignError):
             km.kmassign_plan(1000, 300, 64, **kw)
+
+
+def test_plan_for_a_described_gb300_matches_the_device():
+    """The host-only planner given this GPU's description plans what the
+    device planner plans (GB300: 152 SMs, 232,448 bytes, 76 resident pairs)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    props = torch.cuda.get_device_properties(0)
+    if props.multi_processor_count != 152:
+        pytest.skip("not a 152-SM GB300")
+    for N, K, D in [(4096, 128, 64), (65536, 4096, 128), (262144, 16384, 256),
+                    (1048576, 4096, 128), (65536, 16384, 64), (20000, 700, 64), (777, 300, 192)]:
+        assert km.kmassign_plan_for(N, K, D) == km.kmassign_plan(N, K, D), (N, K, D)
