@@ -293,10 +293,13 @@ int kmassign_centroids(const float *sums, const int32_t *counts, const void *C_o
 /*
  * `iters` Lloyd iterations on the device: each assigns X to C (norms computed
  * inside) into idx, then replaces every centroid that received points by
- * their mean (kmassign_update + kmassign_centroids), in place in C.  On
- * return idx holds the last assignment, made with the centroids before the
- * last update.  Temporaries (sums, counts, norms) come from the library's
- * stream-ordered pool.  iters < 0 returns KMASSIGN_ERR_ARG.
+ * their mean (kmassign_update + kmassign_centroids), in place in C.  Where
+ * the update is the sorted one (N * D >= 2^24), the assignment kernel counts
+ * the points per centroid as it stores idx and the update starts from those
+ * counts; the results are those of the separate calls.  On return idx holds
+ * the last assignment, made with the centroids before the last update.
+ * Temporaries (sums, counts, norms, the sort's scratch) come from the
+ * library's stream-ordered pool.  iters < 0 returns KMASSIGN_ERR_ARG.
  */
 int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int iters,
                    int32_t *idx, void *stream);

@@ -461,7 +461,7 @@ int64_t split_first_row(const Plan &plan)
 
 int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int64_t K, int64_t D,
                int32_t *idx, float *minscore, int force_ksplit, int force_rows, int force_nt,
-               int force_cw, cudaStream_t stream)
+               int force_cw, cudaStream_t stream, int32_t *counts = nullptr)
 {
     int rc = check_shape(N, K, D);
     if (rc != KMASSIGN_OK)
@@ -528,6 +528,7 @@ int run_assign(const void *X, const void *C, const float *cnorm, int64_t N, int6
     if (rc == KMASSIGN_OK) {
         AssignParams p = make_params(plan, cnorm != nullptr ? cnorm : tmp_norm, idx, minscore,
                                      reinterpret_cast<unsigned long long *>(split), N, K, D);
+        p.counts = counts;
         if (split != nullptr)
             p.counters =
                 reinterpret_cast<uint32_t *>(split + kma::split_counter_offset(n_split));
@@ -812,10 +813,12 @@ int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int 
     float *sums = nullptr;
     int32_t *counts = nullptr;
     const size_t sum_bytes = static_cast<size_t>(K) * D * 4;
+    // padded to whole 16-byte groups: the sorted update scans it with 16-byte loads
+    const size_t count_bytes = static_cast<size_t>(kma::update_padded_bins(K)) * 4;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&sums), sum_bytes, dev.pool, s) !=
             cudaSuccess ||
-        cudaMallocFromPoolAsync(reinterpret_cast<void **>(&counts), static_cast<size_t>(K) * 4,
-                                dev.pool, s) != cudaSuccess) {
+        cudaMallocFromPoolAsync(reinterpret_cast<void **>(&counts), count_bytes, dev.pool, s) !=
+            cudaSuccess) {
         if (sums != nullptr)
             cudaFreeAsync(sums, s);
         return KMASSIGN_ERR_CUDA;
@@ -826,19 +829,26 @@ int kmassign_lloyd(const void *X, void *C, int64_t N, int64_t K, int64_t D, int 
             cudaSuccess)
         rc = KMASSIGN_ERR_CUDA;
     for (int it = 0; rc == KMASSIGN_OK && it < iters; ++it) {
-        // assignment with the current centroids (norms computed inside) ...
-        rc = run_assign(X, C, nullptr, N, K, D, idx, nullptr, 0, 0, 0, 0, s);
+        if (cudaMemsetAsync(counts, 0, count_bytes, s) != cudaSuccess) {
+            rc = KMASSIGN_ERR_CUDA;
+            break;
+        }
+        // assignment with the current centroids (norms computed inside); with
+        // the sorted update it also counts the points per centroid as it
+        // stores idx, so the update starts from the scan ...
+        rc = run_assign(X, C, nullptr, N, K, D, idx, nullptr, 0, 0, 0, 0, s,
+                        scratch != nullptr ? counts : nullptr);
         if (rc != KMASSIGN_OK)
             break;
         // ... then the means of the assigned points replace them in place
-        if (cudaMemsetAsync(sums, 0, sum_bytes, s) != cudaSuccess ||
-            cudaMemsetAsync(counts, 0, static_cast<size_t>(K) * 4, s) != cudaSuccess) {
+        if (cudaMemsetAsync(sums, 0, sum_bytes, s) != cudaSuccess) {
             rc = KMASSIGN_ERR_CUDA;
             break;
         }
         const cudaError_t upd =
             scratch != nullptr
-                ? kma::launch_update_sorted(X, idx, N, K, D, sums, counts, scratch, dev.sms, s)
+                ? kma::launch_update_sorted_counted(X, idx, N, K, D, sums, counts, scratch,
+                                                    dev.sms, s)
                 : kma::launch_update(X, idx, N, K, D, sums, counts, dev.sms, s);
         if (upd != cudaSuccess ||
             kma::launch_centroids(sums, counts, C, K, D, C, nullptr, s) != cudaSuccess)

@@ -127,6 +127,8 @@ __device__ __forceinline__ void merge_split_group(const AssignParams &p, int row
             float ms;
             unpack_key(__ldcg(p.keys + rel), ix, ms);
             p.idx[row] = ix;
+            if (p.counts != nullptr)
+                atomicAdd(p.counts + ix, 1);
             if (p.minscore != nullptr)
                 p.minscore[row] = ms;
         }
@@ -403,6 +405,8 @@ __global__ void __launch_bounds__(32 * (4 * SUB * CH + 4), 1)
                             ms = (__float_as_uint(best) == 0x80000000u) ? 0.0f : best;
                         }
                         p.idx[row] = ix;
+                        if (p.counts != nullptr)
+                            atomicAdd(p.counts + ix, 1);
                         if (p.minscore != nullptr)
                             p.minscore[row] = ms;
                     }
@@ -939,6 +943,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                             ms = (__float_as_uint(best) == 0x80000000u) ? 0.0f : best;
                         }
                         p.idx[row] = ix;
+                        if (p.counts != nullptr)
+                            atomicAdd(p.counts + ix, 1);
                         if (p.minscore != nullptr)
                             p.minscore[row] = ms;
                     }

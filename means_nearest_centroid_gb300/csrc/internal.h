@@ -28,6 +28,9 @@ struct AssignParams {
     // before the launch): the last of a group's ksplit units turns its keys
     // into idx and minscore.
     uint32_t *counters;
+    // Optional (the Lloyd loop): counts[idx[i]] += 1 for every point stored,
+    // the update's histogram formed by the assignment itself.
+    int32_t *counts;
     int32_t topk;                  // k of the k-nearest kernel (idx, minscore hold [N, k])
     const float *xnorm;            // [N] ||x||^2: the k-nearest kernel writes distances
     int32_t N, K, D;
@@ -112,6 +115,13 @@ size_t update_sorted_scratch_bytes(int64_t N, int64_t K);
 cudaError_t launch_update_sorted(const void *X, const int32_t *idx, int64_t N, int64_t K,
                                  int64_t D, float *sums, int32_t *counts, void *scratch, int sms,
                                  cudaStream_t stream);
+// The sorted update when counts already holds the histogram of idx (the
+// assignment formed it): counts has update_padded_bins(K) entries, 16-byte
+// aligned, zero past K; only sums is accumulated.
+int64_t update_padded_bins(int64_t K);
+cudaError_t launch_update_sorted_counted(const void *X, const int32_t *idx, int64_t N, int64_t K,
+                                         int64_t D, float *sums, const int32_t *counts,
+                                         void *scratch, int sms, cudaStream_t stream);
 cudaError_t launch_centroids(const float *sums, const int32_t *counts, const void *C_old, int64_t K,
                              int64_t D, void *C_new, float *means, cudaStream_t stream);
 // score[i] = max(xnorm[i] + score[i], 0) (NaN kept): distances from scores.

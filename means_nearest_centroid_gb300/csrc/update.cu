@@ -194,6 +194,15 @@ __device__ void last_block_scans(uint32_t *ticket, const int32_t *hist, int64_t 
     scan_bins_block(hist, Kp, cursor, total_out, warp_sums);
 }
 
+// The scan alone, by one block (K <= kSmallScanMax), when the histogram was
+// formed elsewhere (by the assignment kernel in the Lloyd loop).
+__global__ void __launch_bounds__(kScanThreads)
+    scan_kernel(const int32_t *hist, int64_t Kp, int32_t *cursor, int32_t *total)
+{
+    __shared__ int64_t warp_sums[33];
+    scan_bins_block(hist, Kp, cursor, total, warp_sums);
+}
+
 // hist[j] += 1 for every point with a valid id; with scan, the last block
 // then scans the bins.
 __global__ void __launch_bounds__(kScanThreads)
@@ -388,7 +397,7 @@ __global__ void __launch_bounds__(256)
         float *dst = sums + static_cast<int64_t>(cur) * D + part * 8;
         red_add_v4(dst, acc[0], acc[1], acc[2], acc[3]);
         red_add_v4(dst + 4, acc[4], acc[5], acc[6], acc[7]);
-        if (part == 0)
+        if (counts != nullptr && part == 0)
             atomicAdd(counts + cur, n);
     };
     for (int64_t s0 = begin; s0 < end; s0 += kAhead) {
@@ -429,6 +438,102 @@ __global__ void __launch_bounds__(256)
         flush();
 }
 
+// The counting sort's placement and the run reductions (counts may be NULL:
+// the histogram was formed elsewhere).
+cudaError_t scatter_and_sum(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
+                            float *sums, int32_t *counts, int32_t *cursor, int2 *perm,
+                            const int32_t *total, bool local, int64_t lblocks, int64_t lper,
+                            size_t lsmem, int sms, cudaStream_t stream)
+{
+    const int threads = 256;
+    if (local)
+        block_scatter_kernel<<<static_cast<unsigned>(lblocks), 1024, lsmem, stream>>>(
+            idx, N, static_cast<int32_t>(K), lper, cursor, perm);
+    else
+        scatter_kernel<<<static_cast<unsigned>(
+                             (N + int64_t(threads) * kPerThread - 1) / (int64_t(threads) * kPerThread)),
+                         threads, 0, stream>>>(idx, N, static_cast<int32_t>(K), cursor, perm);
+    // Runs of R points: enough groups to give every SM about 48 resident warps.
+    const int vec = static_cast<int>(D / 8);
+    const int per_warp = 32 / vec;
+    const int64_t groups_target = int64_t(sms) * 48 * per_warp;
+    int64_t R = (N + groups_target - 1) / groups_target;
+    R = std::max<int64_t>(kAhead, (R + kAhead - 1) / kAhead * kAhead);
+    const int64_t groups = (N + R - 1) / R;
+    const int64_t warps = (groups + per_warp - 1) / per_warp;
+    const int64_t sblocks = (warps * 32 + threads - 1) / threads;
+    segsum_kernel<<<static_cast<unsigned>(sblocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(X), perm, total, static_cast<int32_t>(D),
+        static_cast<int32_t>(R), sums, counts);
+    return cudaGetLastError();
+}
+
+// counted == nullptr: count, scan, scatter and sum, adding the counts into
+// counts.  counted != nullptr: the histogram is given (padded, zero past K);
+// scan it, scatter and sum (counts unused).
+cudaError_t launch_update_sorted_impl(const void *X, const int32_t *idx, int64_t N, int64_t K,
+                                      int64_t D, float *sums, int32_t *counts,
+                                      const int32_t *counted, void *scratch, int sms,
+                                      cudaStream_t stream)
+{
+    // scratch: [ticket 16 B][hist Kp][cursor Kp][perm 2N][tile offsets][total]
+    const int64_t ntiles = (K + kScanTile - 1) / kScanTile;
+    const int64_t Kp = padded_bins(K);
+    uint8_t *p = static_cast<uint8_t *>(scratch);
+    uint32_t *ticket = reinterpret_cast<uint32_t *>(p);
+    int32_t *hist = reinterpret_cast<int32_t *>(p + 16);
+    int32_t *cursor = hist + Kp;
+    int2 *perm = reinterpret_cast<int2 *>(cursor + Kp);   // Kp is even: 8-byte aligned
+    uint8_t *tail = reinterpret_cast<uint8_t *>(perm + N);
+    int64_t *tile_off = reinterpret_cast<int64_t *>(
+        (reinterpret_cast<uintptr_t>(tail) + 7) & ~uintptr_t(7));
+    int32_t *total = reinterpret_cast<int32_t *>(tile_off + ntiles);
+    const bool one_block_scan = K <= kSmallScanMax;
+    // Block-local counting when blocks of about 4K points each (so nearly
+    // every bin of a block is hit, and the global atomics drop about 4x) still
+    // give at least 32 blocks.
+    const int64_t lblocks = std::min<int64_t>(int64_t(sms) * 2, N / (4 * K));
+    const bool local = K <= kLocalMaxBins && lblocks >= 32;
+    const int64_t lper = local ? (N + lblocks - 1) / lblocks : 0;
+    const size_t lsmem = static_cast<size_t>(K) * 4;
+    if (counted != nullptr) {
+        if (one_block_scan)
+            scan_kernel<<<1, kScanThreads, 0, stream>>>(counted, Kp, cursor, total);
+        else {
+            tile_sum_kernel<<<static_cast<unsigned>(ntiles), kScanThreads, 0, stream>>>(
+                counted, static_cast<int32_t>(K), tile_off);
+            tile_offsets_kernel<<<1, kScanThreads, 0, stream>>>(tile_off, ntiles);
+            scan_apply_kernel<<<static_cast<unsigned>(ntiles), kScanThreads, 0, stream>>>(
+                counted, static_cast<int32_t>(K), tile_off, cursor, total);
+        }
+        return scatter_and_sum(X, idx, N, K, D, sums, nullptr, cursor, perm, total, local, lblocks,
+                               lper, lsmem, sms, stream);
+    }
+    // One memset clears the ticket and the padded bins.
+    cudaError_t e = cudaMemsetAsync(p, 0, 16 + static_cast<size_t>(Kp) * 4, stream);
+    if (e != cudaSuccess)
+        return e;
+    // With K <= kSmallScanMax the counting kernel's last block scans the bins.
+    const int64_t blocks =
+        (N + int64_t(kScanThreads) * kHistPerThread - 1) / (int64_t(kScanThreads) * kHistPerThread);
+    if (local)
+        block_hist_kernel<<<static_cast<unsigned>(lblocks), kScanThreads, lsmem, stream>>>(
+            idx, N, static_cast<int32_t>(K), lper, hist, one_block_scan, Kp, ticket, cursor,
+            total);
+    else
+        hist_kernel<<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(
+            idx, N, static_cast<int32_t>(K), hist, one_block_scan, Kp, ticket, cursor, total);
+    if (!one_block_scan) {
+        tile_sum_kernel<<<static_cast<unsigned>(ntiles), kScanThreads, 0, stream>>>(
+            hist, static_cast<int32_t>(K), tile_off);
+        tile_offsets_kernel<<<1, kScanThreads, 0, stream>>>(tile_off, ntiles);
+        scan_apply_kernel<<<static_cast<unsigned>(ntiles), kScanThreads, 0, stream>>>(
+            hist, static_cast<int32_t>(K), tile_off, cursor, total);
+    }
+    return scatter_and_sum(X, idx, N, K, D, sums, counts, cursor, perm, total, local, lblocks,
+                           lper, lsmem, sms, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_update(const void *X, const int32_t *idx, int64_t N, int64_t K, int64_t D,
@@ -453,72 +558,25 @@ size_t update_sorted_scratch_bytes(int64_t N, int64_t K)
            8 + static_cast<size_t>(ntiles) * 8 + 64;         // tile offsets, total
 }
 
+int64_t update_padded_bins(int64_t K)
+{
+    return padded_bins(K);
+}
+
+cudaError_t launch_update_sorted_counted(const void *X, const int32_t *idx, int64_t N, int64_t K,
+                                         int64_t D, float *sums, const int32_t *counts,
+                                         void *scratch, int sms, cudaStream_t stream)
+{
+    return launch_update_sorted_impl(X, idx, N, K, D, sums, nullptr, counts, scratch, sms,
+                                     stream);
+}
+
 cudaError_t launch_update_sorted(const void *X, const int32_t *idx, int64_t N, int64_t K,
                                  int64_t D, float *sums, int32_t *counts, void *scratch, int sms,
                                  cudaStream_t stream)
 {
-    // scratch: [ticket 16 B][hist Kp][cursor Kp][perm 2N][tile offsets][total]
-    const int64_t ntiles = (K + kScanTile - 1) / kScanTile;
-    const int64_t Kp = padded_bins(K);
-    uint8_t *p = static_cast<uint8_t *>(scratch);
-    uint32_t *ticket = reinterpret_cast<uint32_t *>(p);
-    int32_t *hist = reinterpret_cast<int32_t *>(p + 16);
-    int32_t *cursor = hist + Kp;
-    int2 *perm = reinterpret_cast<int2 *>(cursor + Kp);   // Kp is even: 8-byte aligned
-    uint8_t *tail = reinterpret_cast<uint8_t *>(perm + N);
-    int64_t *tile_off = reinterpret_cast<int64_t *>(
-        (reinterpret_cast<uintptr_t>(tail) + 7) & ~uintptr_t(7));
-    int32_t *total = reinterpret_cast<int32_t *>(tile_off + ntiles);
-    // One memset clears the ticket and the padded bins.
-    cudaError_t e = cudaMemsetAsync(p, 0, 16 + static_cast<size_t>(Kp) * 4, stream);
-    if (e != cudaSuccess)
-        return e;
-    // With K <= kSmallScanMax the counting kernel's last block scans the bins.
-    const bool one_block_scan = K <= kSmallScanMax;
-    const int64_t blocks =
-        (N + int64_t(kScanThreads) * kHistPerThread - 1) / (int64_t(kScanThreads) * kHistPerThread);
-    // Block-local counting when blocks of about 4K points each (so nearly
-    // every bin of a block is hit, and the global atomics drop about 4x) still
-    // give at least 32 blocks.
-    const int64_t lblocks = std::min<int64_t>(int64_t(sms) * 2, N / (4 * K));
-    const bool local = K <= kLocalMaxBins && lblocks >= 32;
-    const int64_t lper = local ? (N + lblocks - 1) / lblocks : 0;
-    const size_t lsmem = static_cast<size_t>(K) * 4;
-    if (local)
-        block_hist_kernel<<<static_cast<unsigned>(lblocks), kScanThreads, lsmem, stream>>>(
-            idx, N, static_cast<int32_t>(K), lper, hist, one_block_scan, Kp, ticket, cursor,
-            total);
-    else
-        hist_kernel<<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(
-            idx, N, static_cast<int32_t>(K), hist, one_block_scan, Kp, ticket, cursor, total);
-    if (!one_block_scan) {
-        tile_sum_kernel<<<static_cast<unsigned>(ntiles), kScanThreads, 0, stream>>>(
-            hist, static_cast<int32_t>(K), tile_off);
-        tile_offsets_kernel<<<1, kScanThreads, 0, stream>>>(tile_off, ntiles);
-        scan_apply_kernel<<<static_cast<unsigned>(ntiles), kScanThreads, 0, stream>>>(
-            hist, static_cast<int32_t>(K), tile_off, cursor, total);
-    }
-    const int threads = 256;
-    if (local)
-        block_scatter_kernel<<<static_cast<unsigned>(lblocks), 1024, lsmem, stream>>>(
-            idx, N, static_cast<int32_t>(K), lper, cursor, perm);
-    else
-        scatter_kernel<<<static_cast<unsigned>(
-                             (N + int64_t(threads) * kPerThread - 1) / (int64_t(threads) * kPerThread)),
-                         threads, 0, stream>>>(idx, N, static_cast<int32_t>(K), cursor, perm);
-    // Runs of R points: enough groups to give every SM about 48 resident warps.
-    const int vec = static_cast<int>(D / 8);
-    const int per_warp = 32 / vec;
-    const int64_t groups_target = int64_t(sms) * 48 * per_warp;
-    int64_t R = (N + groups_target - 1) / groups_target;
-    R = std::max<int64_t>(kAhead, (R + kAhead - 1) / kAhead * kAhead);
-    const int64_t groups = (N + R - 1) / R;
-    const int64_t warps = (groups + per_warp - 1) / per_warp;
-    const int64_t sblocks = (warps * 32 + threads - 1) / threads;
-    segsum_kernel<<<static_cast<unsigned>(sblocks), threads, 0, stream>>>(
-        static_cast<const uint4 *>(X), perm, total, static_cast<int32_t>(D),
-        static_cast<int32_t>(R), sums, counts);
-    return cudaGetLastError();
+    return launch_update_sorted_impl(X, idx, N, K, D, sums, counts, nullptr, scratch, sms,
+                                     stream);
 }
 
 }  // namespace kma

@@ -198,3 +198,29 @@ def test_update_sorted_many_scan_tiles(dev):
     assert np.array_equal(sums[torch.from_numpy(touched).to(dev)].cpu().double().numpy(),
                           o_sums[touched])
     assert float(sums.abs().sum()) == float(np.abs(o_sums).sum())
+
+
+@pytest.mark.parametrize("N,K,D", [
+    (70000, 600, 256),      # sorted update, one-block scan, global scatter
+    (131072, 256, 128),     # N >> K: block-local counting sort
+    (66000, 70000, 256),    # K > 65,536: the scan takes three kernels
+])
+def test_lloyd_sorted_update_matches_host_driven_pieces(dev, N, K, D):
+    """Sizes where the Lloyd loop takes the sorted update (N * D >= 2^24):
+    the assignment counts the points per centroid as it stores idx, and the
+    update starts from the scan of those counts.  On integer data every sum is
+    exact, so two iterations must give the bits of the same steps made
+    through the public calls (assignment, sorted update, new centroids)."""
+    assert N * D >= 1 << 24
+    X, C0 = workloads.integers(N, K, D, seed=N + K)
+    Xd = X.to(dev)
+    C_loop = C0.to(dev).clone()
+    idx_loop = km.kmassign_lloyd(Xd, C_loop, iters=2)
+    assert km.kmassign_check() == 0
+    C = C0.to(dev).clone()
+    for _ in range(2):
+        idx = km.kmassign(Xd, C)
+        sums, counts = km.kmassign_update(Xd, idx, K, method=2)
+        km.kmassign_centroids(sums, counts, C, C_new=C)
+    assert torch.equal(idx_loop, idx)
+    assert torch.equal(C_loop.view(torch.int16), C.view(torch.int16))
