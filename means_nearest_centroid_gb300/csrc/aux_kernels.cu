@@ -30,11 +30,15 @@ __global__ void __launch_bounds__(32 * kNormWarps)
     norms_kernel(const uint4 *__restrict__ C, int64_t K, int32_t D, float *__restrict__ cnorm)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t j = static_cast<int64_t>(blockIdx.x) * kNormWarps + (threadIdx.x >> 5);
-    if (j >= K)
-        return;
-    const float acc = warp_row_norm(C + j * (D >> 3), D, lane);
-    if (lane == 0)
+    const int rpw = rows_per_warp(D);
+    const int64_t row0 =
+        (static_cast<int64_t>(blockIdx.x) * kNormWarps + (threadIdx.x >> 5)) * rpw;
+    if (row0 >= K)
+        return;   // uniform across the warp
+    const float acc = warp_rows_norm(C, row0, K, D, lane);
+    const int vpr = rpw == 1 ? 32 : D >> 3;
+    const int64_t j = row0 + lane / vpr;
+    if (lane % vpr == 0 && j < K)
         cnorm[j] = acc;
 }
 
@@ -47,6 +51,7 @@ struct PrepArgs {
     int64_t K, rows, fill_words;
     int64_t row_blocks;      // blocks [0, row_blocks) work on centroid rows
     int32_t D;
+    int32_t rpw;             // rows per warp: 32 with the caller's norms, else rows_per_warp(D)
 };
 
 // Rows: one warp per centroid row j < rows (rows covers K, and the fold
@@ -69,17 +74,24 @@ __global__ void __launch_bounds__(32 * kNormWarps) prep_kernel(const PrepArgs a)
         return;
     }
     const int lane = threadIdx.x & 31;
-    const int64_t j = static_cast<int64_t>(blockIdx.x) * kNormWarps + (threadIdx.x >> 5);
-    if (j >= a.rows)
-        return;
+    const int64_t row0 =
+        (static_cast<int64_t>(blockIdx.x) * kNormWarps + (threadIdx.x >> 5)) * a.rpw;
+    if (row0 >= a.rows)
+        return;   // uniform across the warp
+    // lanes per row: one with the caller's norms, else D / 8 (the whole warp
+    // for a single row)
+    const int lpr = a.cnorm_in != nullptr ? 1 : (a.rpw == 1 ? 32 : a.D >> 3);
+    const int64_t j = row0 + lane / lpr;
     float norm = __int_as_float(0x7fc00000);
-    if (j < a.K) {
-        if (a.cnorm_in != nullptr)
+    if (a.cnorm_in != nullptr) {
+        if (j < a.K)
             norm = __ldg(a.cnorm_in + j);
-        else
-            norm = warp_row_norm(a.C + j * (a.D >> 3), a.D, lane);
+    } else {
+        const float acc = warp_rows_norm(a.C, row0, a.K, a.D, lane);
+        if (j < a.K)
+            norm = acc;
     }
-    if (lane != 0)
+    if (lane % lpr != 0 || j >= a.rows)
         return;
     if (a.cnorm_out != nullptr && j < a.K)
         a.cnorm_out[j] = norm;
@@ -179,9 +191,17 @@ cudaError_t launch_centroids(const float *sums, const int32_t *counts, const voi
     return cudaGetLastError();
 }
 
+// rows_per_warp on the host
+static int rows_per_warp_host(int D)
+{
+    const int v = D >> 3;
+    return (v < 32 && (v & (v - 1)) == 0) ? 32 / v : 1;
+}
+
 cudaError_t launch_norms(const void *C, int64_t K, int64_t D, float *cnorm, cudaStream_t stream)
 {
-    const int64_t blocks = (K + kNormWarps - 1) / kNormWarps;
+    const int64_t rows_per_block = int64_t(kNormWarps) * rows_per_warp_host(static_cast<int>(D));
+    const int64_t blocks = (K + rows_per_block - 1) / rows_per_block;
     norms_kernel<<<static_cast<unsigned>(blocks), 32 * kNormWarps, 0, stream>>>(
         static_cast<const uint4 *>(C), K, static_cast<int32_t>(D), cnorm);
     return cudaGetLastError();
@@ -203,7 +223,9 @@ cudaError_t launch_prep(const void *C, int64_t K, int64_t D, const float *cnorm_
     a.rows = std::max<int64_t>(cnorm_out != nullptr ? K : 0,
                                fold != nullptr ? fold_operand_blocks(K) * 128 : 0);
     a.fill_words = fill != nullptr ? static_cast<int64_t>(fill_bytes / 16) : 0;
-    a.row_blocks = (a.rows + kNormWarps - 1) / kNormWarps;
+    a.rpw = cnorm_in != nullptr ? 32 : rows_per_warp_host(static_cast<int>(D));
+    const int64_t rows_per_block = int64_t(kNormWarps) * a.rpw;
+    a.row_blocks = (a.rows + rows_per_block - 1) / rows_per_block;
     const int64_t fill_blocks =
         std::min<int64_t>((a.fill_words + 32 * kNormWarps - 1) / (32 * kNormWarps), 1024);
     const int64_t blocks = a.row_blocks + fill_blocks;

@@ -44,6 +44,44 @@ __device__ __forceinline__ float warp_row_norm(const uint4 *__restrict__ row, in
     return acc;
 }
 
+// Rows of a warp: 32 / (D / 8) rows when D / 8 is a power of two below 32
+// (D = 16, 32, 64, 128), one otherwise.
+__device__ __forceinline__ int rows_per_warp(int D)
+{
+    const int v = D >> 3;
+    return (v < 32 && (v & (v - 1)) == 0) ? 32 / v : 1;
+}
+
+// ||c_j||^2 for the rows_per_warp(D) rows row0 .. of a warp, D / 8 lanes per
+// row (lane l: row row0 + l / (D / 8), vector l % (D / 8)); rows at or past K
+// sum nothing.  The lanes of a row combine by the same xor tree as
+// warp_row_norm restricted to the row's lanes -- the offsets it leaves out
+// only add +0 there -- so the bits are warp_row_norm's.  Every lane returns
+// its row's sum.
+__device__ __forceinline__ float warp_rows_norm(const uint4 *__restrict__ C, int64_t row0, int64_t K,
+                                                int D, int lane)
+{
+    const int vpr = D >> 3;
+    if (rows_per_warp(D) == 1)
+        return row0 < K ? warp_row_norm(C + row0 * vpr, D, lane) : 0.0f;
+    const int64_t j = row0 + lane / vpr;
+    float acc = 0.0f;
+    if (j < K) {
+        const uint4 q = __ldg(C + j * vpr + lane % vpr);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = __uint_as_float(w[i] << 16);
+            const float hi = __uint_as_float(w[i] & 0xffff0000u);
+            acc = fmaf(lo, lo, acc);
+            acc = fmaf(hi, hi, acc);
+        }
+    }
+    for (int off = vpr >> 1; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    return acc;
+}
+
 __device__ __forceinline__ uint32_t bf16_bits(float v)
 {
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
