@@ -269,14 +269,17 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const int64_t P = v.pair ? dev.pair_clusters : dev.sms;   // units run in parallel
         // Shared memory: at least 2 ring stages and one X buffer; two X
         // buffers when 4 stages still fit; then as many stages as fit.
+        // A folding CTA pair's ring holds whole tiles (groups of kblocks
+        // stages, at least two groups).
         const size_t budget = static_cast<size_t>(dev.smem_optin);
         auto fits = [&](int st, int xb) { return smem_of(v, kblocks, st, xb) <= budget; };
-        if (!fits(2, 1))
+        const int group = topk ? 1 : kma::assign_stage_group(v, kblocks);
+        if (!fits(2 * group, 1))
             continue;
-        const int xbufs = fits(4, 2) ? 2 : 1;
-        int stages = 2;
-        while (stages < kma::kMaxStages && fits(stages + 1, xbufs))
-            ++stages;
+        const int xbufs = fits(std::max(4, 2 * group), 2) ? 2 : 1;
+        int stages = 2 * group;
+        while (stages + group <= kma::kMaxStages && fits(stages + group, xbufs))
+            stages += group;
         const int64_t ntiles = cdiv(K, v.nt);
         const int64_t R = cdiv(N, static_cast<int64_t>(rows));
         const double mma_clk = v.nt == 256 ? 128.0 : (v.sub == 2 ? 80.0 : 92.0);
@@ -440,7 +443,7 @@ AssignParams make_params(const Plan &plan, const float *cnorm, int32_t *idx, flo
     p.ntiles = plan.ntiles;
     p.num_units = plan.units;
     p.stages = plan.stages;
-    p.fold_stages = kma::pair_fold_stages(p.kblocks, plan.stages);
+    p.stage_group = kma::assign_stage_group(plan.v, p.kblocks);
     p.xbufs = plan.xbufs;
     p.timeout_ns = g_wait_timeout_ns.load();
     return p;

@@ -477,6 +477,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     // t = -s / 2.  Here the pair's N = 256 MMAs leave the tensor pipe room
     // for the extra step, and the lighter reduction is what sets the pace.
     constexpr bool kFold = KB <= 2;
+    // Folded, one full/empty barrier pair covers a whole tile: its KB C
+    // k-block halves and its fold rows.  A tcgen05.commit that completes a
+    // barrier phase costs the tensor pipe ~30-45 clocks on GB300 (measured
+    // with commits to barriers that do and do not complete a phase), and so
+    // does each wait of the issuing thread; per-tile grouping leaves one
+    // commit and one wait for the ring where per-k-block barriers and a
+    // separate fold ring took KB + 1 of each, against a tile of only 5 or 9
+    // MMA steps.  Above D = 128 a tile has 12 or 16 MMA steps and its
+    // k-blocks keep a barrier pair each, so that the ring can refill at
+    // k-block granularity.
+    constexpr int kGroupKB = kFold ? KB : 1;   // C k-blocks per barrier pair
     constexpr int kCW = NT / CH;
     constexpr int kChunks = kCW / 32;
     constexpr int kGroup = kChunks < 4 ? kChunks : 4;
@@ -495,10 +506,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     const uint32_t x_base = base;
     const uint32_t c_base = x_base + p.xbufs * kXBufBytes;
     const uint32_t cn_base = c_base + p.stages * kCStageBytes;
-    // fold: the ones tile, then p.fold_stages fold slots; else the norm ring
+    // C stage groups (p.stages is a multiple of kGroupKB)
+    const uint32_t ngroups = static_cast<uint32_t>(p.stages / kGroupKB);
+    // fold: the ones tile, then one fold slot per stage group; else the norm
+    // ring
     const uint32_t norm_bytes =
-        kFold ? kOnesBytes + static_cast<uint32_t>(p.fold_stages) * kFoldBlockBytes
-              : kCnStages * NT * 4u;
+        kFold ? kOnesBytes + ngroups * kFoldBlockBytes : kCnStages * NT * 4u;
     const uint32_t red_base = cn_base + norm_bytes;
     const uint32_t snap_base = red_base + (CH - 1) * kTileM * 8;
     const uint32_t thr_base = snap_base + (kSnap ? kConsumerWarps * 4096u : 0u);
@@ -517,7 +530,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     const bool leader = rank == 0;
     // The leader's copy of barrier i, as a cluster address.
     auto lead_bar = [&](int i) -> uint32_t { return map_to_rank(bar(i), 0); };
-    if (!debug_layout_ok(p, bar_base - raw + kMiscBytes))
+    if (!debug_layout_ok(p, bar_base - raw + kMiscBytes) ||
+        !debug_ok(p.stage_group == kGroupKB && p.stages % kGroupKB == 0))
         return;   // both CTAs of the pair decide alike
 
     if (threadIdx.x == 0) {
@@ -537,13 +551,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
         for (int s = 0; s < kCnStages; ++s) {
             mbar_init(bar(kBarCnFull + s), 32);
             mbar_init(bar(kBarCnEmpty + s), kConsumerWarps);
-        }
-        for (int s = 0; s < kMaxStages; ++s) {
-            // the fold slots' full barriers count the leader's expect_tx and
-            // both CTAs' copied bytes; the pair MMA's commit frees a slot in
-            // both CTAs
-            mbar_init(bar(kBarFoldFull + s), 1);
-            mbar_init(bar(kBarFoldEmpty + s), 1);
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -572,11 +579,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
             if (kFold)
                 tma_prefetch_desc(&fmap);
             const uint64_t pol_c = policy_evict_last();
-            uint32_t stage = 0, phase = 0, fold_n = 0;
+            // folded: stage = the stage group, else the stage
+            uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int u = cluster; ok && u < p.num_units; u += nclusters) {
                 const Unit w = decode_unit<2>(p, u);
                 for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
+                    if constexpr (kFold) {
+                        // The tile's group: its KB k-block halves of C and
+                        // this CTA's 128 centroids of the fold operand
+                        // (block 2 * tile + rank, 256 rows of 16 bytes), all
+                        // counted on one full barrier of the leader.
+                        if (!(ok = wait1(bar(kBarCEmpty + stage), phase ^ 1u, abort_flag,
+                                         p.timeout_ns)))
+                            break;
+                        if (leader)
+                            mbar_arrive_expect_tx(bar(kBarCFull + stage),
+                                                  2 * (KB * kCStageBytes + kFoldBlockBytes));
+#pragma unroll
+                        for (int kb = 0; kb < KB; ++kb)
+                            tma_load_2d_pair(c_base + (stage * KB + kb) * kCStageBytes, &cmap,
+                                             lead_bar(kBarCFull + stage), kb * kKBlock,
+                                             tile * NT + static_cast<int>(rank) * kHalf, pol_c);
+                        tma_load_2d_pair(cn_base + kOnesBytes + stage * kFoldBlockBytes, &fmap,
+                                         lead_bar(kBarCFull + stage), 0,
+                                         (2 * tile + static_cast<int>(rank)) * 256, pol_c);
+                        if (++stage == ngroups) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb) {
                         if (!(ok = wait1(bar(kBarCEmpty + stage), phase ^ 1u, abort_flag,
@@ -591,21 +624,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                             stage = 0;
                             phase ^= 1u;
                         }
-                    }
-                    if (kFold && ok) {
-                        // this CTA's 128 centroids of the tile: fold block
-                        // 2 * tile + rank, 256 rows of 16 bytes
-                        const uint32_t fs = fold_n % static_cast<uint32_t>(p.fold_stages);
-                        const uint32_t fph = (fold_n / static_cast<uint32_t>(p.fold_stages)) & 1u;
-                        if (!(ok = wait1(bar(kBarFoldEmpty + fs), fph ^ 1u, abort_flag,
-                                         p.timeout_ns)))
-                            break;
-                        if (leader)
-                            mbar_arrive_expect_tx(bar(kBarFoldFull + fs), 2 * kFoldBlockBytes);
-                        tma_load_2d_pair(cn_base + kOnesBytes + fs * kFoldBlockBytes, &fmap,
-                                         lead_bar(kBarFoldFull + fs), 0,
-                                         (2 * tile + static_cast<int>(rank)) * 256, pol_c);
-                        ++fold_n;
                     }
                 }
             }
@@ -654,7 +672,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
         __syncwarp();
     } else if (warp == kMmaWarp) {
         if (leader) {
-            uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0, fold_used = 0;
+            // folded: stage = the stage group, else the stage
+            uint32_t stage = 0, phase = 0, x_used = 0, acc_used = 0;
             bool ok = true, issued = false;
             const uint64_t ones_desc = kFold ? plain_kmajor_desc(cn_base, kFoldLbo, kFoldSbo) : 0;
             for (int u = cluster; ok && u < p.num_units; u += nclusters) {
@@ -670,27 +689,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                 for (int tile = w.t_begin; ok && tile < w.t_end; ++tile) {
                     const uint32_t as = acc_used & 1u;
                     const uint32_t aph = (acc_used >> 1) & 1u;
-                    const uint32_t fb = fold_used % static_cast<uint32_t>(p.fold_stages);
-                    const uint32_t fph = (fold_used / static_cast<uint32_t>(p.fold_stages)) & 1u;
-                    if (kFold) {
+                    if constexpr (kFold) {
                         // Folded tiles are short (5 or 9 MMA steps), so the
                         // accumulator hand-off is on the critical path: wait
-                        // for the tile's operands first (the copies run tiles
-                        // ahead), then for the stage, and issue at once.
-                        uint32_t s2 = stage, ph2 = phase;
-#pragma unroll
-                        for (int kb = 0; kb < KB; ++kb) {
-                            if (ok)
-                                ok = wait_warp(bar(kBarCFull + s2), ph2, abort_flag, p.timeout_ns);
-                            if (++s2 == static_cast<uint32_t>(p.stages)) {
-                                s2 = 0;
-                                ph2 ^= 1u;
-                            }
-                        }
-                        if (ok)
-                            ok = wait_warp(bar(kBarFoldFull + fb), fph, abort_flag, p.timeout_ns);
-                        if (!ok)
+                        // for the tile's group first (the copies run tiles
+                        // ahead), then for the stage, and issue at once: the
+                        // k-steps, the fold step (ones x the group's fold
+                        // rows), one commit that frees the group in both
+                        // CTAs and one that hands the stage to the consumers.
+                        if (!(ok = wait_warp(bar(kBarCFull + stage), phase, abort_flag,
+                                             p.timeout_ns)))
                             break;
+                        if (!(ok = wait_warp(bar(kBarAccEmpty + as), aph ^ 1u, abort_flag,
+                                             p.timeout_ns)))
+                            break;
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem_base + as * kAccCols;
+                        const uint64_t bdesc =
+                            plain_kmajor_desc(cn_base + kOnesBytes + stage * kFoldBlockBytes,
+                                              kFoldPairLbo, kFoldPairSbo);
+                        if (elect_one()) {
+#pragma unroll
+                            for (int kb = 0; kb < KB; ++kb) {
+                                const uint64_t cdesc =
+                                    sw128_kmajor_desc(c_base + (stage * KB + kb) * kCStageBytes);
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    mma_bf16_pair(d_tmem, adesc[kb] + 2u * k, cdesc + 2u * k,
+                                                  kIdesc, (kb | k) != 0);
+                            }
+                            mma_bf16_pair(d_tmem, ones_desc, bdesc, kIdesc, 1u);
+                            mma_commit_pair(bar(kBarCEmpty + stage), kBoth);
+                            mma_commit_pair(bar(kBarAccFull + as), kBoth);
+                        }
+                        __syncwarp();
+                        issued = true;
+                        if (++stage == ngroups) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        ++acc_used;
+                        continue;
                     }
                     if (!(ok = wait_warp(bar(kBarAccEmpty + as), aph ^ 1u, abort_flag,
                                          p.timeout_ns)))
@@ -719,17 +758,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                     }
                     if (!ok)
                         break;
-                    if (kFold) {
-                        const uint64_t bdesc =
-                            plain_kmajor_desc(cn_base + kOnesBytes + fb * kFoldBlockBytes,
-                                              kFoldPairLbo, kFoldPairSbo);
-                        if (elect_one()) {
-                            mma_bf16_pair(d_tmem, ones_desc, bdesc, kIdesc, 1u);
-                            mma_commit_pair(bar(kBarFoldEmpty + fb), kBoth);
-                        }
-                        __syncwarp();
-                        ++fold_used;
-                    }
                     if (elect_one())
                         mma_commit_pair(bar(kBarAccFull + as), kBoth);
                     __syncwarp();
@@ -1106,16 +1134,18 @@ const Variant kVariants[kNumVariants] = {{2, 128, 1, false}, {1, 256, 2, false},
                                          {1, 256, 4, false}, {1, 256, 2, true},
                                          {1, 256, 4, true}};
 
-int pair_fold_stages(int kblocks, int stages)
+int assign_stage_group(const Variant &v, int kblocks)
 {
-    return std::min(kMaxStages, std::max(2, (stages + kblocks - 1) / kblocks));
+    return v.pair && assign_folds(v, kblocks) ? kblocks : 1;
 }
 
 size_t assign_smem_bytes(const Variant &v, int kblocks, int stages, int xbufs)
 {
     const size_t stage_rows = v.pair ? v.nt / 2 : v.nt;
     const bool fold = assign_folds(v, kblocks);   // the kernels' kFold
-    const size_t fold_slots = v.pair ? pair_fold_stages(kblocks, stages) : kFoldStages;
+    // a folding pair: one fold slot per stage group (one tile's stages)
+    const size_t fold_slots =
+        v.pair ? static_cast<size_t>(stages / assign_stage_group(v, kblocks)) : kFoldStages;
     const size_t fold_slot = v.pair ? kFoldBlockBytes : static_cast<size_t>(v.nt) * 32;
     const size_t norm_bytes =
         fold ? kOnesBytes + fold_slots * fold_slot : kCnStages * v.nt * 4;

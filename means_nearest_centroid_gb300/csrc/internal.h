@@ -44,7 +44,7 @@ struct AssignParams {
     int32_t ntiles;                // ceil(K / nt)
     int32_t num_units;             // full_units + (rowtiles - split_row0) * ksplit
     int32_t stages;                // shared-memory ring depth
-    int32_t fold_stages;           // CTA pair folding the norms: fold-operand ring depth
+    int32_t stage_group;           // C stages per barrier pair (assign_stage_group)
     int32_t xbufs;                 // X tile buffers (1 or 2)
     uint64_t timeout_ns;           // bound on every pipeline wait
 };
@@ -84,9 +84,9 @@ bool assign_folds(const Variant &v, int kblocks);
 // centroids, 4 KiB each ([K half][128 rows][16 B] bf16), written from the
 // norms by launch_prep (rows past K hold NaN).
 int64_t fold_operand_blocks(int64_t K);
-// Fold-operand slots of a folding CTA pair with `stages` C stages: one per
-// tile the C ring holds (at least 2, at most kMaxStages).
-int pair_fold_stages(int kblocks, int stages);
+// C stages per barrier pair of the shape: a folding CTA pair groups the
+// k-blocks of a tile (its ring depth is a multiple of this), others use 1.
+int assign_stage_group(const Variant &v, int kblocks);
 size_t fold_operand_bytes(int64_t K);
 
 // The k-nearest kernel: one shape (256 points x 128 centroids per tile, 8

@@ -39,9 +39,7 @@ constexpr int kBarCEmpty = kBarCFull + kMaxStages;    // [kMaxStages]
 constexpr int kCnStages = 4;                          // centroid-norm ring depth
 constexpr int kBarCnFull = kBarCEmpty + kMaxStages;   // [kCnStages]
 constexpr int kBarCnEmpty = kBarCnFull + kCnStages;   // [kCnStages]
-constexpr int kBarFoldFull = kBarCnEmpty + kCnStages; // [kMaxStages] CTA pair's fold ring
-constexpr int kBarFoldEmpty = kBarFoldFull + kMaxStages;   // [kMaxStages]
-constexpr int kNumBars = kBarFoldEmpty + kMaxStages;
+constexpr int kNumBars = kBarCnEmpty + kCnStages;
 constexpr uint32_t kMiscBytes = kNumBars * 8 + 16;    // + tmem slot, abort flag, 2 split flags
 // Norm folding (every assignment kernel at D <= 128, the k-nearest kernel at
 // every D): the norms enter the accumulator through one more K = 16 MMA step
@@ -55,10 +53,9 @@ constexpr uint32_t kFoldLbo = 128;                    // between the two core ma
 constexpr uint32_t kFoldSbo = 256;                    // between 8-row groups
 // The CTA pair's fold operand comes from global memory by TMA, one block of
 // 128 centroids (4 KiB) per CTA and tile, laid out [K half][128 rows][16 B]:
-// the same unswizzled K-major core matrices with other offsets.  Its ring has
-// a slot per tile the C ring can hold (pair_fold_stages), so the producer,
-// which loads a tile's C k-blocks and then its fold block, never waits for a
-// fold slot before the C ring is full.
+// the same unswizzled K-major core matrices with other offsets.  It has one
+// slot per group of C stages (the stages of one tile), loaded and freed with
+// the group.
 constexpr uint32_t kFoldBlockBytes = 4096;
 constexpr uint32_t kFoldPairLbo = 2048;               // between the two K halves
 constexpr uint32_t kFoldPairSbo = 128;                // between 8-row groups
@@ -110,8 +107,7 @@ __device__ __forceinline__ bool debug_layout_ok(const AssignParams &p, uint32_t 
     if (!kDebugChecks)
         return true;
     const bool ok = layout_end <= dynamic_smem_bytes() && p.stages >= 2 &&
-                    p.stages <= kMaxStages && p.xbufs >= 1 && p.xbufs <= kMaxXBufs &&
-                    p.fold_stages >= 2 && p.fold_stages <= kMaxStages && p.ksplit >= 1 &&
+                    p.stages <= kMaxStages && p.xbufs >= 1 && p.xbufs <= kMaxXBufs && p.ksplit >= 1 &&
                     p.chunk_tiles >= 1 && p.ntiles >= 1;
     if (!ok && threadIdx.x == 0)
         debug_ok(false);
