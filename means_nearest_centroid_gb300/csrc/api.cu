@@ -226,7 +226,7 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 //     tile with 4 warps;
 //   * a CTA pair costs its measured tile time: above D = 128 the larger of
 //     its MMA time and floor, scaled by 0.94; at D <= 128, where it folds,
-//     ~1390 (D = 64) / ~1420 (D = 128) clocks with 8 warps, plus ~4000
+//     ~1050 (D = 64) / ~1380 (D = 128) clocks with 8 warps, plus ~4000
 //     clocks per call for the fold operand (written by the preparation
 //     launch, which computes the norms too when the caller gives none);
 //   * a unit pays ~5000 clocks to load its X tile and fill the pipe;
@@ -283,12 +283,11 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         const int64_t ntiles = cdiv(K, v.nt);
         const int64_t R = cdiv(N, static_cast<int64_t>(rows));
         const double mma_clk = v.nt == 256 ? 128.0 : (v.sub == 2 ? 80.0 : 92.0);
-        // Kernels that fold the norms into one more MMA step (single-block
-        // at D <= 64, CTA pairs at D <= 128) have a lighter reduction
-        // (256x128 single-block tiles at D = 64: ~1,500 clocks with 8 warps,
-        // ~1,600 with 16; a CTA pair's 128x256 per SM: ~1,390 at D = 64 and
-        // ~1,420 at D = 128, against ~1,780 for the 256x128 single block at
-        // D = 128).
+        // Kernels that fold the norms into one more MMA step (every shape at
+        // D <= 128) have a lighter reduction (256x128 single-block tiles at
+        // D = 64: ~1,500 clocks with 8 warps, ~1,600 with 16; a CTA pair's
+        // 128x256 per SM: ~1,050 at D = 64 and ~1,380 at D = 128, against
+        // ~1,780 for the 256x128 single block at D = 128).
         const bool fold = !topk && kma::assign_folds(v, kblocks);
         const double tile_mma = double(v.sub) * (kblocks * 4 + (fold ? 1 : 0)) * mma_clk + 500.0;
         const double tile_epi =
@@ -305,11 +304,14 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
         // cap (less L2 traffic per flop).  At D <= 128 it folds, modelled
         // by its reduction floor above.
         const double pair_factor = kblocks >= 3 ? 0.94 : 1.0;
-        // A folding pair's tile is its measured time (8 warps: ~1,390 clocks
-        // at D = 64, ~1,420 at D = 128), below its modelled MMA time; its
-        // fold operand costs one small kernel per call.
+        // A folding pair's tile is its fitted time (8 warps: ~1,050 clocks
+        // at D = 64, ~1,380 at D = 128, since its tiles take one ring wait
+        // and two commits), below its modelled MMA time; its fold operand
+        // costs one small kernel per call.  Fitted so that the pair is chosen
+        // from ~2,048 centroids up at D = 64, where it measured 7-12% faster
+        // than the single block, and single blocks below.
         const bool pair_fold = v.pair && fold;
-        const double tile = pair_fold ? (v.ch == 2 ? (kblocks == 1 ? 1390.0 : 1420.0) : 1600.0)
+        const double tile = pair_fold ? (v.ch == 2 ? (kblocks == 1 ? 1050.0 : 1380.0) : 1600.0)
                                       : std::max(tile_mma, tile_epi) * (v.pair ? pair_factor : 1.0);
         const double call_over = pair_fold ? 4000.0 : 0.0;
         const double unit_over = 5000.0;

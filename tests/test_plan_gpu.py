@@ -60,9 +60,13 @@ def test_pair_plans_are_chosen_for_large_shapes(dev):
     for D in (256, 192, 128, 96, 64):
         p = km.kmassign_plan(262144, 16384, D)
         assert (p["rows_per_cta"], p["centroids_per_tile"]) == (256, 256), D
-    # short centroid ranges at D = 64 stay on the single-block fold
+    # short centroid ranges at D = 64 stay on the single-block fold, longer
+    # ones from ~2,048 centroids go to the pair
+    for N, K in [(262144, 512), (262144, 1024), (65536, 512)]:
+        p = km.kmassign_plan(N, K, 64)
+        assert (p["rows_per_cta"], p["centroids_per_tile"]) == (256, 128), (N, K)
     p = km.kmassign_plan(262144, 4096, 64)
-    assert (p["rows_per_cta"], p["centroids_per_tile"]) == (256, 128)
+    assert (p["rows_per_cta"], p["centroids_per_tile"]) == (256, 256)
     # every shape can be forced at any D
     p = km.kmassign_plan(65536, 4096, 32, rows_per_cta=256, centroids_per_tile=256,
                          consumer_warps=8)
