@@ -486,7 +486,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
     // separate fold ring took KB + 1 of each, against a tile of only 5 or 9
     // MMA steps.  Above D = 128 a tile has 12 or 16 MMA steps and its
     // k-blocks keep a barrier pair each, so that the ring can refill at
-    // k-block granularity.
+    // k-block granularity (pairs of k-blocks per barrier at D = 256 measured
+    // 6-17% slower on the long shapes, the ring then holding 4 stages
+    // instead of 5).
     constexpr int kGroupKB = kFold ? KB : 1;   // C k-blocks per barrier pair
     constexpr int kCW = NT / CH;
     constexpr int kChunks = kCW / 32;
