@@ -39,6 +39,11 @@ def _valid(p, N, K, D, dev):
     if pair:
         assert p["grid"] % 2 == 0 and p["grid"] // 2 <= min(dev["pair_clusters"], dev["sms"] // 2)
     assert 2 <= p["stages"] <= 16 and p["xbufs"] in (1, 2), p
+    if pair and D <= 128:
+        # a folding pair's ring holds whole tiles: a multiple of the tile's
+        # k-blocks (one barrier pair each), at least two tiles
+        kb = -(-D // 64)
+        assert p["stages"] % kb == 0 and p["stages"] >= 2 * kb, p
     rowtiles = -(-max(N, 1) // rows)
     assert p["whole_row_tiles"] + p["split_row_tiles"] == rowtiles, p
     assert p["ksplit"] >= 1
