@@ -21,7 +21,7 @@
         }                                                                                         \
     } while (0)
 
-static int plan_ok(const int32_t *p, int64_t N, int64_t K, int sms, int pairs)
+static int plan_ok(const int32_t *p, int64_t N, int64_t K, int64_t D, int sms, int pairs)
 {
     const int rows = p[1], nt = p[2], cw = p[8];
     const int pair = rows == 256 && nt == 256;
@@ -31,6 +31,11 @@ static int plan_ok(const int32_t *p, int64_t N, int64_t K, int sms, int pairs)
     if (p[3] < 1 || p[3] > sms || (pair && (p[3] % 2 != 0 || p[3] / 2 > pairs)))
         return 0;
     if (p[4] < 2 || p[4] > 16 || (p[5] != 1 && p[5] != 2))
+        return 0;
+    /* a folding pair's ring holds whole tiles: a multiple of the k-blocks,
+       at least two tiles */
+    const int kb = (int)((D + 63) / 64);
+    if (pair && D <= 128 && (p[4] % kb != 0 || p[4] < 2 * kb))
         return 0;
     const int64_t rowtiles = ((N < 1 ? 1 : N) + rows - 1) / rows;
     if ((int64_t)p[6] + p[7] != rowtiles || p[0] < 1 || (p[0] > 1) != (p[7] > 0))
@@ -114,7 +119,7 @@ int main(void)
                                     if (rc == KMASSIGN_ERR_ARG)
                                         continue;
                                     CHECK(rc == KMASSIGN_OK, "plan_for status");
-                                    CHECK(plan_ok(p, Ns[a], Ks[b], devs[dv][0], devs[dv][2]),
+                                    CHECK(plan_ok(p, Ns[a], Ks[b], Ds[c], devs[dv][0], devs[dv][2]),
                                           "plan is runnable");
                                     ++plans;
                                 }
