@@ -114,6 +114,9 @@ int run_host(const void *X, const void *C, const float *cnorm, int64_t N, int64_
         (rc = kma::assign_wave_rows(N, K, D, &wave)) != KMASSIGN_OK)
         return rc;
     const int64_t rows = slice_rows(N, wave, rows_per_slice);
+    // Nothing overlaps the first slice's copy, so unless the caller fixed the
+    // slices the first one is a single wave (when the others hold more).
+    const int64_t first_rows = rows_per_slice > 0 ? rows : std::min(rows, wave);
 
     HostPath &h = g_host[dev];
     std::lock_guard<std::mutex> lock(h.mutex);
@@ -158,9 +161,9 @@ int run_host(const void *X, const void *C, const float *cnorm, int64_t N, int64_
         }
     }
     const uint8_t *xh = static_cast<const uint8_t *>(X);
-    for (int64_t s = 0, b0 = 0; rc == KMASSIGN_OK && b0 < N; ++s, b0 += rows) {
+    for (int64_t s = 0, b0 = 0, nr = 0; rc == KMASSIGN_OK && b0 < N; ++s, b0 += nr) {
         const int slot = static_cast<int>(s & 1);
-        const int64_t nr = std::min(rows, N - b0);
+        nr = std::min(s == 0 ? first_rows : rows, N - b0);
         void *xs = static_cast<uint8_t *>(xd) + static_cast<size_t>(slot) * rows * row_bytes;
         int32_t *is = idxd + static_cast<size_t>(slot) * rows;
         float *ms = msd != nullptr ? msd + static_cast<size_t>(slot) * rows : nullptr;
