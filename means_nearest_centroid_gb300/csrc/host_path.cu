@@ -78,7 +78,8 @@ int check_host_ptrs(const void *const *ptrs, int n)
 }
 
 // Rows per slice: the caller's, else about N / kSlices rounded to whole waves
-// (at least one), so that no slice but the last ends in a partly filled wave.
+// (at least one), so that no slice but the last ends in a partly filled wave
+// (run_host makes the first slice a single wave).
 int64_t slice_rows(int64_t N, int64_t wave, int64_t forced)
 {
     if (forced > 0)
