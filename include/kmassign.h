@@ -153,7 +153,8 @@ int kmassign_ex(const void *X, const void *C, const float *cnorm, int64_t N, int
  * alignment is required.  Device pointers return KMASSIGN_ERR_NOT_HOST.
  *
  * C (and cnorm) is copied first; X follows in row slices of about N / 8
- * points, rounded to whole waves of the assignment kernel's thread blocks,
+ * points, rounded to whole waves of the assignment kernel's thread blocks
+ * (the first slice, whose copy nothing overlaps, is a single wave),
  * through two device buffers: the copy of one slice overlaps the assignment
  * of the previous one, and each slice's answers are copied back while the
  * next slice runs.  Each slice is one kmassign call, so the results are
