@@ -77,11 +77,16 @@ __device__ __forceinline__ unsigned long long pack_key(float s, int j)
     return (static_cast<unsigned long long>(o) << 32) | static_cast<uint32_t>(j);
 }
 
-// The (index, score) a packed key stands for; the initial all-ones key (no
-// number seen: every score NaN) gives index 0 and NaN.
+// Key of a unit that saw no number (every score NaN): above every real key
+// (whose high word is at most that of +inf), below the initial all-ones.
+constexpr unsigned long long kKeyNoNumber = ~1ull;
+
+// The (index, score) a packed key stands for; a key with an all-ones high
+// word (the initial value, or kKeyNoNumber: no number seen, every score NaN)
+// gives index 0 and NaN.
 __device__ __forceinline__ void unpack_key(unsigned long long key, int &ix, float &ms)
 {
-    if (key == ~0ull) {
+    if ((key >> 32) == 0xffffffffull) {
         ix = 0;
         ms = __int_as_float(0x7fc00000);
         return;
@@ -91,14 +96,33 @@ __device__ __forceinline__ void unpack_key(unsigned long long key, int &ix, floa
     ms = __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
 }
 
+// The row's answer from its merged key: idx, the histogram count, minscore.
+__device__ __forceinline__ void store_split_row(const AssignParams &p, int row,
+                                                unsigned long long key)
+{
+    int ix;
+    float ms;
+    unpack_key(key, ix, ms);
+    p.idx[row] = ix;
+    if (p.counts != nullptr)
+        atomicAdd(p.counts + ix, 1);
+    if (p.minscore != nullptr)
+        p.minscore[row] = ms;
+}
+
 // Split rows, at the end of a unit, by all 128 consumer threads of one group
 // of 128 rows (bar_id: a named barrier of theirs; flag: a shared word of
-// theirs): merge this unit's winners into the packed keys, then count the
-// unit in at the group's counter.  The counter starts at all-ones and the
-// group's rows are split into p.ksplit units, so the unit that reads
-// ksplit - 2 is the last; it turns the group's keys into idx and minscore.
-// Each thread fences its atomic before the count, and the last unit fences
-// before it reads the keys from L2.
+// theirs).  Every key starts at all-ones.
+// - Two units per row (p.ksplit == 2, the usual tail split): each thread
+//   merges its winner (kKeyNoNumber when it saw no number) with one atomicMin
+//   and gets the key it replaced.  Anything but all-ones there is the other
+//   unit's winner, already merged, so this thread holds both and stores the
+//   row; the atomic's own order on the one key is the whole protocol.
+// - More units per row: merge this unit's winners into the packed keys, then
+//   count the unit in at the group's counter.  The counter starts at
+//   all-ones, so the unit that reads ksplit - 2 is the last; it turns the
+//   group's keys into idx and minscore.  Each thread fences its atomic before
+//   the count, and the last unit fences before it reads the keys from L2.
 __device__ __forceinline__ void merge_split_group(const AssignParams &p, int rows_per_unit,
                                                   int row, bool store, float best, int bi,
                                                   uint32_t bar_id, volatile uint32_t *flag,
@@ -111,6 +135,15 @@ __device__ __forceinline__ void merge_split_group(const AssignParams &p, int row
         store = store && debug_ok(rel >= 0 && rel < n_split);
         counts = counts && debug_ok(rel >= 0 && (rel >> 7) < (n_split + 127) / 128);
     }
+    if (p.ksplit == 2) {
+        if (store) {
+            const unsigned long long mine = bi == kNone ? kKeyNoNumber : pack_key(best, bi);
+            const unsigned long long old = atomicMin(p.keys + rel, mine);
+            if (old != ~0ull)
+                store_split_row(p, row, old < mine ? old : mine);
+        }
+        return;
+    }
     if (store && bi != kNone)
         atomicMin(p.keys + rel, pack_key(best, bi));
     __threadfence();
@@ -122,16 +155,8 @@ __device__ __forceinline__ void merge_split_group(const AssignParams &p, int row
     named_bar_sync(bar_id, 128);
     if (*flag != 0u) {
         __threadfence();
-        if (store) {
-            int ix;
-            float ms;
-            unpack_key(__ldcg(p.keys + rel), ix, ms);
-            p.idx[row] = ix;
-            if (p.counts != nullptr)
-                atomicAdd(p.counts + ix, 1);
-            if (p.minscore != nullptr)
-                p.minscore[row] = ms;
-        }
+        if (store)
+            store_split_row(p, row, __ldcg(p.keys + rel));
     }
 }
 

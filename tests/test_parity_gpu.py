@@ -137,6 +137,49 @@ def test_adversarial_reduced_bit_exact(dev):
         assert rep.ok() and rep.idx_mismatches == 0, (plan, rep)
 
 
+SPLIT_PLANS = [
+    dict(ksplit=2, rows_per_cta=128, centroids_per_tile=256),
+    dict(ksplit=2, rows_per_cta=256, centroids_per_tile=256, consumer_warps=8),
+    dict(ksplit=-2, rows_per_cta=256, centroids_per_tile=256, consumer_warps=8),
+    dict(ksplit=3, rows_per_cta=256, centroids_per_tile=256, consumer_warps=8),
+    dict(ksplit=4, rows_per_cta=256, centroids_per_tile=128),
+]
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("nan_range", ["first", "last", "both"])
+def test_split_ranges_that_see_no_number(dev, D, nan_range):
+    """Split centroid ranges where one range, or every range, sees only NaN
+    scores (centroids holding a NaN), and rows that are NaN themselves: the
+    merged answer is the other range's winner, or idx 0 with a NaN score.
+    Integer data, so every plan must match the oracle and each other bit for
+    bit, whichever unit of a row finishes first."""
+    N, K = 3000, 2048
+    X, C = workloads.integers(N, K, D, seed=D + 5)
+    X[7] = float("nan")
+    X[2999, 3] = float("nan")
+    half = K // 2
+    if nan_range in ("first", "both"):
+        C[:half, 0] = float("nan")
+    if nan_range in ("last", "both"):
+        C[half:, 1] = float("nan")
+    ref = None
+    for plan in SPLIT_PLANS:
+        idx, ms = run(dev, X, C, plan=plan)
+        rep = parity.compare(X, C, idx, ms, integer=True)
+        assert rep.ok() and rep.idx_mismatches == 0, (plan, rep)
+        if nan_range == "both":
+            assert bool((idx == 0).all()) and bool(torch.isnan(ms).all()), plan
+        elif nan_range == "first":
+            finite = ~torch.isnan(X.float()).any(1)
+            assert bool((idx[finite] >= half).all()), plan
+        if ref is None:
+            ref = (idx, ms)
+            continue
+        assert torch.equal(idx, ref[0]), plan
+        assert torch.equal(ms.view(torch.int32), ref[1].view(torch.int32)), plan
+
+
 @pytest.mark.parametrize("D", [96, 128, 192, 256])
 def test_adversarial_specials_every_plan_wider_rows(dev, D):
     """Ties, twins, all-equal centroids and rows with NaN, +-inf and -0 on
