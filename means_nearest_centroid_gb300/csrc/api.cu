@@ -231,8 +231,9 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 //     launch, which computes the norms too when the caller gives none);
 //   * a unit pays ~5000 clocks to load its X tile and fill the pipe;
 //   * any split pays ~5000 clocks: the keys' initial values (the same
-//     preparation launch) and the arrival count at the end of each split
-//     unit, whose last unit turns the keys into the answers.
+//     preparation launch) and the merge at the end of each split unit (one
+//     atomic per row for two ranges; with more, an arrival count whose last
+//     unit turns the keys into the answers).
 // Splits considered: every row tile into ks centroid ranges (ks >= 1), or
 // only the row tiles of the last partial wave (the rest stay whole), which
 // evens out the last wave when there are a few waves of whole row tiles.
