@@ -635,21 +635,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * (4 * CH + 4), 1
                             stage = 0;
                             phase ^= 1u;
                         }
-                        continue;
-                    }
+                    } else {
 #pragma unroll
-                    for (int kb = 0; kb < KB; ++kb) {
-                        if (!(ok = wait1(bar(kBarCEmpty + stage), phase ^ 1u, abort_flag,
-                                         p.timeout_ns)))
-                            break;
-                        if (leader)
-                            mbar_arrive_expect_tx(bar(kBarCFull + stage), 2 * kCStageBytes);
-                        tma_load_2d_pair(c_base + stage * kCStageBytes, &cmap,
-                                         lead_bar(kBarCFull + stage), kb * kKBlock,
-                                         tile * NT + static_cast<int>(rank) * kHalf, pol_c);
-                        if (++stage == static_cast<uint32_t>(p.stages)) {
-                            stage = 0;
-                            phase ^= 1u;
+                        for (int kb = 0; kb < KB; ++kb) {
+                            if (!(ok = wait1(bar(kBarCEmpty + stage), phase ^ 1u, abort_flag,
+                                             p.timeout_ns)))
+                                break;
+                            if (leader)
+                                mbar_arrive_expect_tx(bar(kBarCFull + stage), 2 * kCStageBytes);
+                            tma_load_2d_pair(c_base + stage * kCStageBytes, &cmap,
+                                             lead_bar(kBarCFull + stage), kb * kKBlock,
+                                             tile * NT + static_cast<int>(rank) * kHalf, pol_c);
+                            if (++stage == static_cast<uint32_t>(p.stages)) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
                         }
                     }
                 }

@@ -25,8 +25,9 @@ struct AssignParams {
     // (row, centroid range) for the k-nearest kernel.
     unsigned long long *keys;
     // Arrival counters of the split rows, one per group of 128 (all-ones
-    // before the launch): the last of a group's ksplit units turns its keys
-    // into idx and minscore.
+    // before the launch): with more than two units per row, the last of a
+    // group's ksplit units turns its keys into idx and minscore (two units
+    // merge through the keys alone).
     uint32_t *counters;
     // Optional (the Lloyd loop): counts[idx[i]] += 1 for every point stored,
     // the update's histogram formed by the assignment itself.
