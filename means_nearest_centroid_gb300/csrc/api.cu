@@ -233,7 +233,12 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 //   * any split pays ~5000 clocks: the keys' initial values (the same
 //     preparation launch) and the merge at the end of each split unit (one
 //     atomic per row for two ranges; with more, an arrival count whose last
-//     unit turns the keys into the answers).
+//     unit turns the keys into the answers).  The variant is chosen with
+//     that flat cost; within the chosen variant a split into two ranges is
+//     then re-weighed at ~3000 clocks (kTwoRangeSplitCost, below), since
+//     its merge is one atomic per row.  Re-weighing before the variant
+//     choice tipped some shapes from a CTA pair to single blocks, which
+//     measured slower.
 // Splits considered: every row tile into ks centroid ranges (ks >= 1), or
 // only the row tiles of the last partial wave (the rest stay whole), which
 // evens out the last wave when there are a few waves of whole row tiles.
@@ -242,6 +247,11 @@ int64_t units_of_block(int64_t X, int64_t P, int64_t b) { return X > b ? (X - b 
 // x 128 tiles) and shared-memory layout; its epilogue cost per tile depends on
 // the data and is taken as the assignment's, which only matters for choosing
 // the split.
+// A two-range split's cost in the re-weighing below: on the shapes whose plan
+// it changes (a whole plan becoming a tail split in 2, N 65,536-524,288) the
+// new plans measured level to 5.5% faster.
+constexpr double kTwoRangeSplitCost = 3000.0;
+
 int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_ksplit,
               int force_rows, int force_nt, int force_cw, bool topk, Plan *out,
               bool no_pair = false)
@@ -254,6 +264,17 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
     bool found = false;
     double best_cost = 0.0;
     Plan best{};
+    // The re-weighed cost of the plan chosen so far, its variant, and each
+    // variant's two-range split candidates (at most two: every row tile, or
+    // the last wave's) with their re-weighed costs.
+    double best_cost2 = 0.0;
+    int best_vi = 0;
+    struct TwoRange {
+        double cost2;
+        Plan plan;
+    };
+    TwoRange two_range[kma::kNumVariants][2];
+    int n_two_range[kma::kNumVariants] = {};
     const kma::Variant *variants = topk ? &kma::kTopkVariant : kma::kVariants;
     const int nvariants = topk ? 1 : kma::kNumVariants;
     for (int vi = 0; vi < nvariants; ++vi) {
@@ -343,22 +364,33 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
                 worst = std::max(worst, c);
             }
             const double cost = worst + (any_split ? 5000.0 : 0.0) + call_over;
-            if (!found || cost < best_cost * 0.995) {
+            const bool two = any_split && ks_eff == 2;
+            const double cost2 = two ? worst + kTwoRangeSplitCost + call_over : cost;
+            const bool take = !found || cost < best_cost * 0.995;
+            if (!take && !(two && !topk))
+                return;
+            Plan c{};
+            c.v = v;
+            c.ksplit = any_split ? static_cast<int>(ks_eff) : 1;
+            c.rowtiles = static_cast<int>(R);
+            c.ntiles = static_cast<int>(ntiles);
+            c.chunk_tiles = any_split ? static_cast<int>(chunk) : static_cast<int>(ntiles);
+            c.full_units = static_cast<int>(full_units);
+            c.split_row0 = static_cast<int>(split_row0);
+            c.units = static_cast<int>(nunits);
+            c.grid = static_cast<int>(std::min<int64_t>(nunits, P) * (v.pair ? 2 : 1));
+            c.stages = stages;
+            c.xbufs = xbufs;
+            c.smem = smem_of(v, kblocks, stages, xbufs);
+            if (take) {
                 found = true;
                 best_cost = cost;
-                best.v = v;
-                best.ksplit = any_split ? static_cast<int>(ks_eff) : 1;
-                best.rowtiles = static_cast<int>(R);
-                best.ntiles = static_cast<int>(ntiles);
-                best.chunk_tiles = any_split ? static_cast<int>(chunk) : static_cast<int>(ntiles);
-                best.full_units = static_cast<int>(full_units);
-                best.split_row0 = static_cast<int>(split_row0);
-                best.units = static_cast<int>(nunits);
-                best.grid = static_cast<int>(std::min<int64_t>(nunits, P) * (v.pair ? 2 : 1));
-                best.stages = stages;
-                best.xbufs = xbufs;
-                best.smem = smem_of(v, kblocks, stages, xbufs);
+                best_cost2 = cost2;
+                best_vi = vi;
+                best = c;
             }
+            if (two && !topk && n_two_range[vi] < 2)
+                two_range[vi][n_two_range[vi]++] = TwoRange{cost2, c};
         };
         if (force_ksplit > 0) {
             const int64_t ks = std::min<int64_t>(force_ksplit, ntiles);
@@ -380,6 +412,17 @@ int make_plan(int64_t N, int64_t K, int64_t D, const DeviceInfo &dev, int force_
     }
     if (!found)
         return KMASSIGN_ERR_ARG;
+    // The variant stays the one chosen above; within it, a two-range split
+    // replaces the plan when its re-weighed cost is lower by the same margin.
+    if (force_ksplit == 0) {
+        for (int i = 0; i < n_two_range[best_vi]; ++i) {
+            const TwoRange &t = two_range[best_vi][i];
+            if (t.cost2 < best_cost2 * 0.995) {
+                best_cost2 = t.cost2;
+                best = t.plan;
+            }
+        }
+    }
     *out = best;
     return KMASSIGN_OK;
 }
