@@ -103,3 +103,33 @@ def test_argument_errors():
     with pytest.raises(km.KmassignError) as e:
         km.kmassign_plan_for(10, 10, 64, smem_per_block=1024)
     assert e.value.code == S["KMASSIGN_ERR_ARG"]
+
+
+def _shape(p):
+    return (p["ksplit"], p["rows_per_cta"], p["centroids_per_tile"], p["consumer_warps"],
+            p["whole_row_tiles"])
+
+
+@pytest.mark.parametrize("N,K,D,plan", [
+    # the five workloads: the reported figures were measured on these plans
+    (4096, 128, 64, (1, 128, 128, 4, 32)),               # tiny_blobs
+    (65536, 4096, 128, (2, 256, 256, 8, 228)),           # sampled_centroids: pair, tail split 2
+    (262144, 16384, 256, (2, 256, 256, 8, 988)),         # iid_normal (the bench)
+    (1048576, 4096, 128, (1, 256, 256, 8, 4096)),        # lognormal_clusters: pair, whole
+    (65536, 16384, 64, (2, 256, 256, 8, 228)),           # adversarial_ties: pair, tail split 2
+])
+def test_workload_plans_on_a_gb300(N, K, D, plan):
+    assert _shape(km.kmassign_plan_for(N, K, D)) == plan
+
+
+@pytest.mark.parametrize("N,K,D,plan", [
+    # a two-range split re-weighed within the chosen shape: whole pair row
+    # tiles become a tail split in 2 (measured faster) ...
+    (262144, 2048, 128, (2, 256, 256, 8, 988)),
+    (65536, 1024, 256, (2, 256, 256, 8, 228)),
+    # ... but it never tips the shape: this one stays on whole CTA-pair row
+    # tiles, where single blocks with a tail split measured 18% slower
+    (131072, 1024, 128, (1, 256, 256, 8, 512)),
+])
+def test_two_range_split_keeps_the_shape(N, K, D, plan):
+    assert _shape(km.kmassign_plan_for(N, K, D)) == plan
